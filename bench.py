@@ -1,0 +1,501 @@
+"""Benchmark of the low-precision DDA allreduce emulation on one GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+the LP flat allreduce and the LP tree allreduce (quantize, FP32 reduce,
+requantize, all-gather) of 8 emulated ranks x 67,108,864 FP32 elements
+(256 MiB per rank), the gradient-sized workload. Inputs (2 GiB) are larger
+than L2 (129 MB), so no flush is needed between steps.
+
+value        whole-job GB/s: algorithmic bytes of all steps on all ranks /
+             max-over-ranks time (CUDA events on the launching stream).
+e2e          the same metric through the public API with pinned host
+             buffers: per step, host->device copy of the 8 inputs, both
+             allreduces, device->host copy of both results.
+roofline     the dominant kernel's algorithmic bytes per launch / its average
+             launch time against the measured HBM copy bandwidth.
+cpu_baseline the CPU oracle on a bounded sample of the same workload.
+decode       exact-precision flat allreduce of a decode-size message (8 ranks
+             x 32 x 8192 BF16): single-launch and CUDA-graph replay time.
+workloads    the other reference workloads, GB/s and us per call.
+
+``--impl reference`` times the CPU oracle (the reference arm of this
+benchmark) on a bounded sample of the same workload per step.
+Run with torchrun for N > 1: each rank runs an independent replica (the
+emulation does not shard across GPUs), rank 0 prints the line.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from precision_collective_reduction_gb300 import workloads as W  # noqa: E402
+
+HEADLINE = W.LP_GRAD_N8_256MB_F32
+METRIC = "LP allreduce-emulation GB/s"
+CPU_SAMPLE_ELEMS = 1 << 23      # cpu_baseline: first 8 Mi elements of each rank
+REF_BUDGET_ELEMS = 1 << 25      # reference arm: elements per rank over all steps
+E2E_MAX_STEPS = 20
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "precision_collective_reduction_gb300", "csrc", f)
+                  for f in ("lpcoll_device.cuh", "lpcoll_dda.cuh")]
+
+
+# -- algorithmic bytes --------------------------------------------------------
+
+def bytes_alg(nranks, n, elem, block, algo):
+    """Minimum HBM bytes of one emulated allreduce: inputs read once, each
+    rank's FP8 wire (codes + scales) written once, the tree's requantized
+    shard wire written once, N outputs written."""
+    nb = (n + 127) // 128
+    per_rank = n * elem * 2
+    if block:
+        per_rank += n + 4 * nb
+    total = nranks * per_rank
+    if block and algo == "tree":
+        total += n + 4 * nb
+    return total
+
+
+def step_bytes(w, n=None):
+    n = w.n if n is None else n
+    return sum(bytes_alg(w.nranks, n, w.elem_bytes, w.block, a) for a in w.algos)
+
+
+# -- environment ----------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(kernel_key)
+    if not ent or ent.get("source_digest") != kernel_source_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples every 100 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.samples = []
+        self.proc = None
+        self.marks = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.monotonic(), parts))
+
+    def mark(self):
+        self.marks.append(time.monotonic())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if len(inside) < 3:  # short timed region: widen to the whole GPU phase
+            inside = [p for _, p in self.samples]
+            window = "run"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "samples": 0}
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        smax = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[4 + i].lower() == "active"})
+        pw = [num(p[2]) for p in inside if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max(pw) if pw else None}
+
+
+# -- CPU oracle legs ------------------------------------------------------------
+
+def oracle_pass(w, n):
+    """One flat + tree pass of the CPU oracle over n elements per rank drawn
+    with the workload's recipe and seed; returns seconds."""
+    import oracle
+    ins = [x[:n].copy() for x in W.draw_all(w, n)]
+    t0 = time.perf_counter()
+    for algo in w.algos:
+        (oracle.tree if algo == "tree" else oracle.flat)(ins, block=w.block)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w):
+    secs = oracle_pass(w, CPU_SAMPLE_ELEMS)
+    return {"value": round(step_bytes(w, CPU_SAMPLE_ELEMS) / secs / 1e9, 4),
+            "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d of the workload's %d elements per rank (same recipe and "
+                      "seed), %d ranks, one flat + one tree pass, single-threaded C "
+                      "oracle (%.1f s)"
+                      % (CPU_SAMPLE_ELEMS, w.n, w.nranks, secs)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = HEADLINE
+    n = REF_BUDGET_ELEMS // (args.steps + args.warmup)
+    n = max(64 * 128, min(1 << 20, n // 128 * 128))
+    for _ in range(args.warmup):
+        oracle_pass(w, n)
+    secs = [oracle_pass(w, n) for _ in range(args.steps)]
+    total = sum(secs)
+    value = step_bytes(w, n) * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w, world),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": "%d of the workload's %d elements per rank (same "
+                                   "recipe and seed), %d ranks, flat + tree per step"
+                                   % (n, w.n, w.nranks)},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, world):
+    return {"workload": w.name, "nranks_emulated": w.nranks, "elems_per_rank": w.n,
+            "dtype": "f32" if w.dtype == W.F32 else "bf16", "block": w.block,
+            "algos": list(w.algos), "parallelism": "replicas x%d" % world,
+            "l2": "inputs larger than L2 (%d MiB of inputs per step)"
+                  % (w.nranks * w.message_bytes >> 20)}
+
+
+# -- GPU legs -------------------------------------------------------------------
+
+def timed_steps(torch, bufs, w, stream, steps, warmup, dist, clocks):
+    s = stream.cuda_stream
+    for _ in range(warmup):
+        for a in w.algos:
+            bufs.run(a, s)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(w.algos) + 1)]
+          for _ in range(steps)]
+    t0 = time.monotonic()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            ev[i][0].record(stream)
+            for j, a in enumerate(w.algos):
+                bufs.run(a, s)
+                ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    per_kernel = {a: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)]
+                  for j, a in enumerate(w.algos)}
+    total_ms = ev[0][0].elapsed_time(ev[-1][-1])
+    if dist is not None:
+        dist.barrier()
+    return total_ms, per_kernel, (t0, t1)
+
+
+def e2e_steps(torch, bufs, w, stream, steps, host_in, host_out):
+    s = stream.cuda_stream
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    outs = {a: (bufs.tree_outs if a == "tree" else bufs.outs) for a in w.algos}
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            for t, h in zip(bufs.ins, host_in):
+                t.copy_(h, non_blocking=True)
+            for a in w.algos:
+                bufs.run(a, s)
+            for a in w.algos:
+                for t, h in zip(outs[a], host_out[a]):
+                    h.copy_(t, non_blocking=True)
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def flush_l2(torch, scratch):
+    scratch.add_(1)
+
+
+def measure_small(torch, w, stream, iters, graph_replays=0):
+    """us per call of workload w (median of iters, L2 flushed before each)."""
+    from precision_collective_reduction_gb300 import runner
+    bufs = runner.RankBuffers(w.nranks, w.n, w.dtype, w.block)
+    bufs.load(W.draw_all(w))
+    scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    s = stream.cuda_stream
+    out = {}
+    for algo in w.algos:
+        for _ in range(3):
+            bufs.run(algo, s)
+        times = []
+        with torch.cuda.stream(stream):
+            for _ in range(iters):
+                flush_l2(torch, scratch)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                bufs.run(algo, s)
+                b.record(stream)
+                b.synchronize()
+                times.append(a.elapsed_time(b) * 1e3)
+        us = statistics.median(times)
+        nbytes = bytes_alg(w.nranks, w.n, w.elem_bytes, w.block, algo)
+        res = {"us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
+               "bytes_alg": nbytes, "l2": "flushed"}
+        if graph_replays:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(graph_replays):
+                    bufs.run(algo, stream.cuda_stream)
+            g.replay()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            res["graph_us_per_call"] = round(a.elapsed_time(b) * 1e3 / graph_replays, 3)
+            res["graph_calls"] = graph_replays
+            res["graph_l2"] = "warm (back-to-back replays)"
+            del g
+        out[algo] = res
+    del bufs, scratch
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = tdist
+    else:
+        torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    from precision_collective_reduction_gb300 import runner
+
+    w = HEADLINE
+    stream = torch.cuda.Stream()
+    host = W.draw_all(w)
+    bufs = runner.RankBuffers(w.nranks, w.n, w.dtype, w.block, separate_tree_out=True)
+    bufs.load(host)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    total_ms, per_kernel, (t0, t1) = timed_steps(torch, bufs, w, stream, args.steps,
+                                                 args.warmup, dist, clocks)
+    clock_info = clocks.summary(t0, t1)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    sbytes = step_bytes(w)
+    value = sbytes * args.steps * world / (total_ms / 1e3) / 1e9
+
+    peak, peak_kind = measured_peaks()
+    avg = {a: statistics.fmean(v) for a, v in per_kernel.items()}
+    dom = max(avg, key=lambda a: avg[a])
+    dom_bytes = bytes_alg(w.nranks, w.n, w.elem_bytes, w.block, dom)
+    achieved = dom_bytes / (avg[dom] / 1e3) / 1e9
+    kernel_key = "dda_kernel<8,f32,%s>" % dom
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": profiled_traffic(kernel_key),
+                "kernel": kernel_key, "peak_kind": peak_kind + " hbm_gbs (copy)",
+                "bytes_alg_per_launch": dom_bytes,
+                "avg_launch_us": round(avg[dom] * 1e3, 2)}
+    kernels = {a: {"avg_us": round(avg[a] * 1e3, 2),
+                   "GBps": round(bytes_alg(w.nranks, w.n, w.elem_bytes, w.block, a)
+                                 / (avg[a] / 1e3) / 1e9, 1),
+                   "frac_of_peak": round(bytes_alg(w.nranks, w.n, w.elem_bytes, w.block, a)
+                                         / (avg[a] / 1e3) / 1e9 / peak, 4)}
+               for a in w.algos}
+
+    # end to end through the public API, pinned host buffers
+    host_in = [torch.from_numpy(x).pin_memory() for x in host]
+    host_out = {a: [torch.empty(w.n, dtype=torch.float32).pin_memory()
+                    for _ in range(w.nranks)] for a in w.algos}
+    e2e_n = min(args.steps, E2E_MAX_STEPS)
+    e2e_ms = e2e_steps(torch, bufs, w, stream, e2e_n, host_in, host_out)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(x.nbytes for x in host)
+    d2h = sum(h.numel() * h.element_size() for a in w.algos for h in host_out[a])
+    e2e = {"value": round(sbytes * e2e_n * world / (e2e_ms / 1e3) / 1e9, 2),
+           "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": round(e2e_ms / e2e_n, 3), "steps": e2e_n}
+    del host_in, host_out, bufs
+    torch.cuda.empty_cache()
+
+    extras = {}
+    if not args.headline_only:
+        extras["decode"] = measure_small(torch, W.DECODE_EXACT_FLAT_N8_BF16, stream,
+                                         iters=50, graph_replays=1000)["flat"]
+        extras["workloads"] = {
+            wl.name: measure_small(torch, wl, stream, iters=20)
+            for wl in (W.LP_FLAT_N2_1M_F32, W.LP_FLAT_N8_16MB_BF16,
+                       W.LP_TREE_N8_64MB_BF16)}
+    clocks.stop()
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w, world),
+        "hbm_frac": round(value / world / peak, 4),
+        "roofline": roofline, "kernels": kernels,
+        "e2e": e2e, "gpu_launches": len(w.algos) * args.steps,
+        "clocks": clock_info,
+    }
+    line.update(extras)
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_profile_case(args):
+    """A few launches of one workload's kernels, for ncu captures: `warmup`
+    untimed launches of each algorithm, then `steps` more."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from precision_collective_reduction_gb300 import runner
+    w = W.BY_NAME[args.profile_case]
+    n = args.elems or w.n
+    algos = [args.algo] if args.algo else list(w.algos)
+    bufs = runner.RankBuffers(w.nranks, n, w.dtype, w.block, separate_tree_out=True)
+    bufs.load(W.draw_all(w, n))
+    s = torch.cuda.current_stream().cuda_stream
+    for _ in range(args.warmup):
+        for a in algos:
+            bufs.run(a, s)
+    for _ in range(args.steps):
+        for a in algos:
+            bufs.run(a, s)
+    torch.cuda.synchronize()
+    print("profile case %s n=%d algos=%s: %d launches" % (
+        w.name, n, ",".join(algos), (args.warmup + args.steps) * len(algos)))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the decode and secondary workload measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=sorted(W.BY_NAME),
+                    help="only run a few launches of this workload (for ncu)")
+    ap.add_argument("--elems", type=int, default=0,
+                    help="with --profile-case: elements per rank (default: full)")
+    ap.add_argument("--algo", choices=["flat", "tree"], default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.profile_case:
+        return run_profile_case(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,150 @@
+/*
+ * lpcoll.h -- C ABI of liblpcoll.so: the data-parallel hot path of a
+ * low-precision (FP8) collective reduction and of the DDA flat / tree
+ * allreduce, with N ranks emulated as N buffers in one GPU's memory.
+ *
+ * The method is the one described on code-journey.com, "RCCLX: AMD GPU
+ * communication, Meta open source" (Portuguese and Korean editions):
+ *   - section "Funcionalidade Principal 1: Acesso Direto a Dados (DDA)":
+ *     DDA flat (every rank reads every other rank's data directly and reduces
+ *     locally) and DDA tree (reduce-scatter, then all-gather, each phase by
+ *     direct access);
+ *   - section "Funcionalidade Principal 2: Coletivos de Baixa Precisao":
+ *     FP8 quantization of FP32 / BF16 payloads for messages of 16 MB and more,
+ *     with FP32 kept for the arithmetic (feature table, rows "Tipos de Dados"
+ *     and "Precisao do Calculo").
+ * The pages fix neither the FP8 format nor the scaling. This library uses:
+ *   - OCP E4M3 codes ("e4m3fn", largest finite 448), rounded to nearest even
+ *     and saturated to +-448;
+ *   - one FP32 scale per block of LPCOLL_BLOCK = 128 consecutive elements:
+ *     s = a / 448 with a = max |x| over the block, codes = e4m3(x * (448 / a));
+ *     a block whose 448 / a overflows (a == 0 or a < ~1.3e-36) gets s = 0 and
+ *     signed-zero codes;
+ *   - dequantized values fl(e4m3 * s), summed in FP32 in the fixed order rank
+ *     0, 1, ..., N-1 starting from rank 0's value, no fused multiply-add;
+ *   - BF16 results rounded to nearest even.
+ *
+ * Conventions shared by every entry point:
+ *   - Every data pointer is a DEVICE pointer into memory the caller owns; the
+ *     library allocates nothing, frees nothing and never synchronizes.
+ *     Every device pointer must be 16-byte aligned (LPCOLL_ERR_ALIGN).
+ *   - Pointer arrays (in[], out[], wire_codes[], ...) are HOST arrays of
+ *     nranks device pointers; they are read during the call only.
+ *   - dtype is LPCOLL_F32 (float) or LPCOLL_BF16 (bfloat16 stored as
+ *     uint16); inputs and outputs of one call share it.
+ *   - n is the element count per rank; any n >= 0 is accepted. A payload of
+ *     n elements is codes[n] (one byte each, element order) plus
+ *     scales[ceil(n / 128)] (block b covers elements [128 b, 128 b + 128)).
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Work is enqueued on it and the call returns at once.
+ *   - Return value: LPCOLL_OK, or an lpcoll_status error found before any
+ *     launch (nothing is enqueued then), or LPCOLL_ERR_CUDA if the launch
+ *     itself failed (lpcoll_last_cuda_error() gives the cudaError_t).
+ *     Checks, in order: dtype / nranks (LPCOLL_ERR_ARG), block
+ *     (LPCOLL_ERR_UNSUPPORTED), n == 0 (LPCOLL_OK, nothing launched, pointers
+ *     not inspected), NULL pointer (LPCOLL_ERR_RANK inside a per-rank array,
+ *     else LPCOLL_ERR_ARG), misalignment (LPCOLL_ERR_ALIGN).
+ *   - An output may be the very same buffer as an input (in place, as the
+ *     pages' allreduce example works); any other overlap between buffers of
+ *     one call is undefined.
+ */
+#ifndef LPCOLL_H
+#define LPCOLL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { LPCOLL_F32 = 0, LPCOLL_BF16 = 1 } lpcoll_dtype;
+
+typedef enum {
+    LPCOLL_OK = 0,
+    LPCOLL_ERR_ARG = 1,         /* bad dtype, nranks, or a NULL pointer */
+    LPCOLL_ERR_ALIGN = 2,       /* a device pointer not 16-byte aligned */
+    LPCOLL_ERR_UNSUPPORTED = 3, /* block size other than 128 (or 0 where allowed) */
+    LPCOLL_ERR_RANK = 4,        /* NULL entry in a per-rank pointer array */
+    LPCOLL_ERR_CUDA = 5         /* the kernel launch failed */
+} lpcoll_status;
+
+#define LPCOLL_MAX_RANKS 16
+#define LPCOLL_BLOCK 128
+
+/* Quantize one rank's message into its FP8 payload (the "wire").
+ * Pages: "Funcionalidade Principal 2", FP8 compression of FP32/BF16 data.
+ *   in      n elements of dtype (device)
+ *   block   must be 128
+ *   codes   out: n bytes, codes[i] = e4m3(in[i] * 448 / a_b)   (device)
+ *   scales  out: ceil(n/128) floats, scales[b] = a_b / 448      (device)   */
+int lp_quantize(const void *in, lpcoll_dtype dtype, size_t n, int block,
+                uint8_t *codes, float *scales, void *stream);
+
+/* Expand one FP8 payload back to dtype: out[i] = cast(e4m3(codes[i]) * s_b).
+ * Pages: the receiving side of the low-precision collectives.
+ *   codes, scales   payload as written by lp_quantize (device)
+ *   out             n elements of dtype (device)                           */
+int lp_dequantize(const uint8_t *codes, const float *scales, size_t n,
+                  int block, void *out, lpcoll_dtype dtype, void *stream);
+
+/* Reduce nranks FP8 payloads into one output: dequantize each, sum in FP32
+ * in rank order 0..nranks-1, cast to dtype.
+ * Pages: "Precisao do Calculo", FP32 kept for the arithmetic.
+ *   codes[r], scales[r]   payload of rank r (host array of device pointers)
+ *   nranks                1..16
+ *   out                   n elements of dtype (device)                     */
+int lp_reduce(const uint8_t *const *codes, const float *const *scales,
+              int nranks, size_t n, int block, void *out, lpcoll_dtype dtype,
+              void *stream);
+
+/* DDA flat allreduce over nranks emulated ranks, one fused launch.
+ * Pages: "Funcionalidade Principal 1", bullet "Algoritmo DDA Flat".
+ *   in[r]           rank r's message, n elements of dtype (device)
+ *   out[r]          rank r's result, n elements of dtype (device); all nranks
+ *                   outputs receive the same values; out[r] == in[r] allowed
+ *   block           0: exact precision, out = cast(sum_r in[r]);
+ *                   128: low precision, each rank's message is quantized into
+ *                   wire_codes[r] / wire_scales[r] (written: the payload a
+ *                   rank would expose to its peers) and the outputs are the
+ *                   FP32 sum of the dequantized payloads
+ *   wire_codes[r]   n bytes (device); ignored (may be NULL) when block == 0
+ *   wire_scales[r]  ceil(n/128) floats (device); ignored when block == 0   */
+int dda_flat_sim(const void *const *in, void *const *out, int nranks,
+                 size_t n, lpcoll_dtype dtype, int block,
+                 uint8_t *const *wire_codes, float *const *wire_scales,
+                 void *stream);
+
+/* DDA tree allreduce: reduce-scatter then all-gather, one fused launch.
+ * Pages: "Funcionalidade Principal 1", bullet "Algoritmo DDA Tree".
+ * Rank r owns shard r, elements [r L, min((r+1) L, n)) with
+ * L = ceil(ceil(n/nranks)/128)*128, so shards are whole blocks.
+ *   in, out, nranks, n, dtype, wire_codes, wire_scales   as dda_flat_sim
+ *   block = 128: phase 1 quantizes each rank's message into its wire;
+ *     phase 2 (reduce-scatter) sums the nranks payloads of each shard in
+ *     FP32 and quantizes the reduced shard again into shard_codes (n bytes)
+ *     and shard_scales (ceil(n/128) floats), indexed like the message;
+ *     phase 3 (all-gather) writes the dequantized shard payload to every
+ *     out[r], so outputs carry one more quantization than dda_flat_sim's.
+ *   block = 0: exact precision, same result as dda_flat_sim with block 0;
+ *     wire and shard pointers are ignored (may be NULL).                   */
+int dda_tree_sim(const void *const *in, void *const *out, int nranks,
+                 size_t n, lpcoll_dtype dtype, int block,
+                 uint8_t *const *wire_codes, float *const *wire_scales,
+                 uint8_t *shard_codes, float *shard_scales, void *stream);
+
+/* Static, NUL-terminated name of a status code (never NULL). */
+const char *lpcoll_status_string(int status);
+
+/* cudaError_t of the most recent LPCOLL_ERR_CUDA returned to this thread
+ * (0 if none). */
+int lpcoll_last_cuda_error(void);
+
+/* Library ABI version: 100 * major + minor. */
+int lpcoll_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LPCOLL_H */

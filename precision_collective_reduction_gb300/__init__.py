@@ -1,0 +1,16 @@
+"""GB300-native low-precision (FP8) collective reduction and DDA flat / tree
+allreduce, with N ranks emulated as N buffers in one GPU's HBM.
+
+The compute path is liblpcoll.so (hand-written CUDA for sm_103a behind the C
+ABI in include/lpcoll.h); this package is its binding (``_binding``), an
+in-place allreduce facade (``allreduce``), the build step (``build``) and the
+seeded workload generators (``workloads``).
+"""
+from ._binding import (BF16, BLOCK, F32, MAX_RANKS, LpcollError, dda_flat_sim,
+                       dda_tree_sim, lib, lp_dequantize, lp_quantize, lp_reduce,
+                       nblocks, status_string)
+from .allreduce import Workspace, allreduce_sim, choose
+
+__all__ = ["BF16", "BLOCK", "F32", "MAX_RANKS", "LpcollError", "Workspace",
+           "allreduce_sim", "choose", "dda_flat_sim", "dda_tree_sim", "lib",
+           "lp_dequantize", "lp_quantize", "lp_reduce", "nblocks", "status_string"]

@@ -1,0 +1,231 @@
+"""ctypes binding of liblpcoll.so, one Python function per C entry point.
+
+Argument marshalling only: each function checks that the torch tensors it is
+given are CUDA, contiguous, of the right dtype and large enough, then passes
+their device pointers, the element count and the CUDA stream to the C call
+of the same name, and raises ``LpcollError`` on a non-zero status. All the
+arithmetic runs in the library's kernels. There is no fallback: if the
+library is missing, every call raises.
+"""
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "liblpcoll.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "lpcoll.h")
+
+F32 = 0
+BF16 = 1
+BLOCK = 128
+MAX_RANKS = 16
+
+STATUS = {0: "LPCOLL_OK", 1: "LPCOLL_ERR_ARG", 2: "LPCOLL_ERR_ALIGN",
+          3: "LPCOLL_ERR_UNSUPPORTED", 4: "LPCOLL_ERR_RANK", 5: "LPCOLL_ERR_CUDA"}
+
+_lib = None
+
+
+class LpcollError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s: %s" % (what, status_string(status)))
+
+
+def lib():
+    """The loaded liblpcoll.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                "liblpcoll.so not found at %s; build it with "
+                "precision_collective_reduction_gb300.build.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, sz, ci = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        pp = ctypes.POINTER(ctypes.c_void_p)
+        L.lp_quantize.argtypes = [vp, ci, sz, ci, vp, vp, vp]
+        L.lp_dequantize.argtypes = [vp, vp, sz, ci, vp, ci, vp]
+        L.lp_reduce.argtypes = [pp, pp, ci, sz, ci, vp, ci, vp]
+        L.dda_flat_sim.argtypes = [pp, pp, ci, sz, ci, ci, pp, pp, vp]
+        L.dda_tree_sim.argtypes = [pp, pp, ci, sz, ci, ci, pp, pp, vp, vp, vp]
+        for f in ("lp_quantize", "lp_dequantize", "lp_reduce", "dda_flat_sim",
+                  "dda_tree_sim", "lpcoll_last_cuda_error", "lpcoll_version"):
+            getattr(L, f).restype = ci
+        L.lpcoll_status_string.argtypes = [ci]
+        L.lpcoll_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(status):
+    s = lib().lpcoll_status_string(int(status)).decode()
+    if status == 5:
+        s += " (cudaError %d)" % lib().lpcoll_last_cuda_error()
+    return s
+
+
+def ptr_array(ptrs):
+    """Host array of device pointers (ints) for a per-rank argument."""
+    ptrs = list(ptrs)
+    return (ctypes.c_void_p * max(len(ptrs), 1))(*ptrs)
+
+
+def _check(st, what):
+    if st != 0:
+        raise LpcollError(st, what)
+
+
+# -- raw calls: device pointers as ints ------------------------------------
+
+def raw_lp_quantize(in_ptr, dtype, n, block, codes_ptr, scales_ptr, stream):
+    _check(lib().lp_quantize(in_ptr, dtype, n, block, codes_ptr, scales_ptr, stream),
+           "lp_quantize")
+
+
+def raw_lp_dequantize(codes_ptr, scales_ptr, n, block, out_ptr, dtype, stream):
+    _check(lib().lp_dequantize(codes_ptr, scales_ptr, n, block, out_ptr, dtype, stream),
+           "lp_dequantize")
+
+
+def raw_lp_reduce(codes_ptrs, scales_ptrs, nranks, n, block, out_ptr, dtype, stream):
+    _check(lib().lp_reduce(ptr_array(codes_ptrs), ptr_array(scales_ptrs), nranks, n,
+                           block, out_ptr, dtype, stream), "lp_reduce")
+
+
+def raw_dda_flat_sim(in_ptrs, out_ptrs, nranks, n, dtype, block, wc_ptrs, ws_ptrs,
+                     stream):
+    _check(lib().dda_flat_sim(ptr_array(in_ptrs), ptr_array(out_ptrs), nranks, n,
+                              dtype, block, ptr_array(wc_ptrs), ptr_array(ws_ptrs),
+                              stream), "dda_flat_sim")
+
+
+def raw_dda_tree_sim(in_ptrs, out_ptrs, nranks, n, dtype, block, wc_ptrs, ws_ptrs,
+                     sc_ptr, ss_ptr, stream):
+    _check(lib().dda_tree_sim(ptr_array(in_ptrs), ptr_array(out_ptrs), nranks, n,
+                              dtype, block, ptr_array(wc_ptrs), ptr_array(ws_ptrs),
+                              sc_ptr, ss_ptr, stream), "dda_tree_sim")
+
+
+# -- torch-tensor calls -----------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError("lpcoll data must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def nblocks(n, block=BLOCK):
+    return (n + block - 1) // block
+
+
+def _stream(stream):
+    if stream is None:
+        return _torch().cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _need(t, what, dtype=None, numel=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % what)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % what)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (what, dtype, t.dtype))
+    if numel is not None and t.numel() < numel:
+        raise ValueError("%s holds %d elements, needs %d" % (what, t.numel(), numel))
+    return t.data_ptr()
+
+
+def lp_quantize(x, codes, scales, block=BLOCK, stream=None):
+    """One rank's message x -> FP8 payload (codes uint8[n], scales f32[ceil(n/128)])."""
+    torch = _torch()
+    n = x.numel()
+    xp = _need(x, "x")
+    cp = _need(codes, "codes", torch.uint8, n)
+    sp = _need(scales, "scales", torch.float32, nblocks(n, block) if block else 0)
+    raw_lp_quantize(xp, dtype_code(x), n, block, cp, sp, _stream(stream))
+    return codes, scales
+
+
+def lp_dequantize(codes, scales, out, block=BLOCK, stream=None):
+    """FP8 payload -> out (float32 or bfloat16, n = out.numel())."""
+    torch = _torch()
+    n = out.numel()
+    op = _need(out, "out")
+    cp = _need(codes, "codes", torch.uint8, n)
+    sp = _need(scales, "scales", torch.float32, nblocks(n, block) if block else 0)
+    raw_lp_dequantize(cp, sp, n, block, op, dtype_code(out), _stream(stream))
+    return out
+
+
+def lp_reduce(codes, scales, out, block=BLOCK, stream=None):
+    """Sum of the dequantized payloads codes[r]/scales[r] (rank order) -> out."""
+    torch = _torch()
+    n = out.numel()
+    op = _need(out, "out")
+    cps = [_need(c, "codes[%d]" % r, torch.uint8, n) for r, c in enumerate(codes)]
+    sps = [_need(s, "scales[%d]" % r, torch.float32, nblocks(n, block) if block else 0)
+           for r, s in enumerate(scales)]
+    if len(cps) != len(sps):
+        raise ValueError("codes and scales must list the same ranks")
+    raw_lp_reduce(cps, sps, len(cps), n, block, op, dtype_code(out), _stream(stream))
+    return out
+
+
+def _rank_args(ins, outs, wire_codes, wire_scales, block):
+    torch = _torch()
+    if len(ins) != len(outs):
+        raise ValueError("one output per input rank")
+    n = ins[0].numel()
+    dt = ins[0].dtype
+    ip = [_need(t, "in[%d]" % r, dt, None) for r, t in enumerate(ins)]
+    if any(t.numel() != n for t in ins):
+        raise ValueError("every rank's message must have the same length")
+    op = [_need(t, "out[%d]" % r, dt, n) for r, t in enumerate(outs)]
+    if block:
+        if wire_codes is None or wire_scales is None:
+            raise ValueError("low precision (block=128) needs wire_codes and wire_scales")
+        wc = [_need(t, "wire_codes[%d]" % r, torch.uint8, n)
+              for r, t in enumerate(wire_codes)]
+        ws = [_need(t, "wire_scales[%d]" % r, torch.float32, nblocks(n, block))
+              for r, t in enumerate(wire_scales)]
+        if len(wc) != len(ins) or len(ws) != len(ins):
+            raise ValueError("one wire payload per rank")
+    else:
+        wc, ws = [], []
+    return n, dtype_code(ins[0]), ip, op, wc, ws
+
+
+def dda_flat_sim(ins, outs, block=BLOCK, wire_codes=None, wire_scales=None,
+                 stream=None):
+    """DDA flat allreduce of the N rank messages ``ins`` into ``outs``."""
+    n, dt, ip, op, wc, ws = _rank_args(ins, outs, wire_codes, wire_scales, block)
+    raw_dda_flat_sim(ip, op, len(ip), n, dt, block, wc, ws, _stream(stream))
+    return outs
+
+
+def dda_tree_sim(ins, outs, block=BLOCK, wire_codes=None, wire_scales=None,
+                 shard_codes=None, shard_scales=None, stream=None):
+    """DDA tree allreduce (reduce-scatter, requantize, all-gather)."""
+    torch = _torch()
+    n, dt, ip, op, wc, ws = _rank_args(ins, outs, wire_codes, wire_scales, block)
+    sc = ss = 0
+    if block:
+        if shard_codes is None or shard_scales is None:
+            raise ValueError("low precision tree needs shard_codes and shard_scales")
+        sc = _need(shard_codes, "shard_codes", torch.uint8, n)
+        ss = _need(shard_scales, "shard_scales", torch.float32, nblocks(n, block))
+    raw_dda_tree_sim(ip, op, len(ip), n, dt, block, wc, ws, sc, ss, _stream(stream))
+    return outs

@@ -1,0 +1,256 @@
+// lpcoll_api.cu -- the extern "C" entry points of liblpcoll.so: argument
+// checks (all done on the host before anything is enqueued), launch sizing,
+// and dispatch to the kernels. The semantics of each call are documented in
+// include/lpcoll.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <initializer_list>
+#include <mutex>
+#include <unordered_map>
+
+#include "lpcoll.h"
+#include "lpcoll_dda.cuh"
+
+namespace lpc {
+
+cudaError_t launch_quantize(const void *in, int dtype, size_t n, uint8_t *codes,
+                            float *scales, cudaStream_t stream);
+cudaError_t launch_dequantize(const uint8_t *codes, const float *scales, size_t n,
+                              void *out, int dtype, cudaStream_t stream);
+cudaError_t launch_reduce(const ReduceParams &p, int nranks, size_t n, void *out,
+                          int dtype, cudaStream_t stream);
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+struct OccKey {
+    const void *fn;
+    int dev;
+    bool operator==(const OccKey &o) const { return fn == o.fn && dev == o.dev; }
+};
+struct OccHash {
+    size_t operator()(const OccKey &k) const
+    {
+        return std::hash<const void *>()(k.fn) ^ (static_cast<size_t>(k.dev) << 1);
+    }
+};
+
+std::mutex g_occ_mutex;
+std::unordered_map<OccKey, int, OccHash> g_wave;  // CTAs in one full wave
+
+int full_wave(const void *kernel)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 1;
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    auto it = g_wave.find(OccKey{kernel, dev});
+    if (it != g_wave.end())
+        return it->second;
+    int sms = 0, per_sm = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+    int wave = sms * per_sm;
+    if (wave < 1)
+        wave = 1;
+    g_wave.emplace(OccKey{kernel, dev}, wave);
+    return wave;
+}
+
+inline bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+inline bool bad_dtype(int dtype) { return dtype != LPCOLL_F32 && dtype != LPCOLL_BF16; }
+
+// NULL / alignment check of one per-rank pointer array.
+template <class P>
+int check_rank_array(P const *arr, int nranks)
+{
+    if (arr == nullptr)
+        return LPCOLL_ERR_ARG;
+    for (int r = 0; r < nranks; ++r)
+        if (arr[r] == nullptr)
+            return LPCOLL_ERR_RANK;
+    for (int r = 0; r < nranks; ++r)
+        if (misaligned(arr[r]))
+            return LPCOLL_ERR_ALIGN;
+    return LPCOLL_OK;
+}
+
+int check_ptr(const void *p)
+{
+    if (p == nullptr)
+        return LPCOLL_ERR_ARG;
+    return misaligned(p) ? LPCOLL_ERR_ALIGN : LPCOLL_OK;
+}
+
+int finish(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return LPCOLL_OK;
+    g_last_cuda_error = static_cast<int>(e);
+    return LPCOLL_ERR_CUDA;
+}
+
+// First non-OK status of a list of checks (NULL before alignment is kept by
+// the order in which callers list them).
+int first_error(std::initializer_list<int> sts)
+{
+    int align = LPCOLL_OK;
+    for (int s : sts) {
+        if (s == LPCOLL_ERR_ALIGN) {
+            if (align == LPCOLL_OK)
+                align = s;
+        } else if (s != LPCOLL_OK) {
+            return s;
+        }
+    }
+    return align;
+}
+
+int dda_common(const void *const *in, void *const *out, int nranks, size_t n,
+               int dtype, int block, uint8_t *const *wire_codes,
+               float *const *wire_scales, uint8_t *shard_codes, float *shard_scales,
+               bool tree, void *stream)
+{
+    if (bad_dtype(dtype) || nranks < 1 || nranks > LPCOLL_MAX_RANKS)
+        return LPCOLL_ERR_ARG;
+    if (block != 0 && block != LPCOLL_BLOCK)
+        return LPCOLL_ERR_UNSUPPORTED;
+    if (n == 0)
+        return LPCOLL_OK;
+    const bool lp = block != 0;
+    int st = first_error({
+        check_rank_array(in, nranks),
+        check_rank_array(out, nranks),
+        lp ? check_rank_array(wire_codes, nranks) : LPCOLL_OK,
+        lp ? check_rank_array(wire_scales, nranks) : LPCOLL_OK,
+        (lp && tree) ? check_ptr(shard_codes) : LPCOLL_OK,
+        (lp && tree) ? check_ptr(shard_scales) : LPCOLL_OK,
+    });
+    if (st != LPCOLL_OK)
+        return st;
+
+    DdaParams p = {};
+    for (int r = 0; r < nranks; ++r) {
+        p.in[r] = in[r];
+        p.out[r] = out[r];
+        if (lp) {
+            p.codes[r] = wire_codes[r];
+            p.scales[r] = wire_scales[r];
+        }
+    }
+    p.shard_codes = (lp && tree) ? shard_codes : nullptr;
+    p.shard_scales = (lp && tree) ? shard_scales : nullptr;
+    const int mode = !lp ? kExact : (tree ? kTree : kFlat);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(dtype == LPCOLL_F32 ? launch_dda_f32(p, nranks, n, mode, s)
+                                      : launch_dda_bf16(p, nranks, n, mode, s));
+}
+
+}  // namespace
+
+int wave_ctas(const void *kernel, size_t units)
+{
+    const size_t need = (units + kWarpsPerCta - 1) / kWarpsPerCta;
+    const size_t wave = static_cast<size_t>(full_wave(kernel));
+    const size_t g = need < wave ? need : wave;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+}  // namespace lpc
+
+using namespace lpc;
+
+extern "C" {
+
+int lp_quantize(const void *in, lpcoll_dtype dtype, size_t n, int block,
+                uint8_t *codes, float *scales, void *stream)
+{
+    if (bad_dtype(dtype))
+        return LPCOLL_ERR_ARG;
+    if (block != LPCOLL_BLOCK)
+        return LPCOLL_ERR_UNSUPPORTED;
+    if (n == 0)
+        return LPCOLL_OK;
+    int st = first_error({check_ptr(in), check_ptr(codes), check_ptr(scales)});
+    if (st != LPCOLL_OK)
+        return st;
+    return finish(launch_quantize(in, dtype, n, codes, scales,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+int lp_dequantize(const uint8_t *codes, const float *scales, size_t n, int block,
+                  void *out, lpcoll_dtype dtype, void *stream)
+{
+    if (bad_dtype(dtype))
+        return LPCOLL_ERR_ARG;
+    if (block != LPCOLL_BLOCK)
+        return LPCOLL_ERR_UNSUPPORTED;
+    if (n == 0)
+        return LPCOLL_OK;
+    int st = first_error({check_ptr(codes), check_ptr(scales), check_ptr(out)});
+    if (st != LPCOLL_OK)
+        return st;
+    return finish(launch_dequantize(codes, scales, n, out, dtype,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+int lp_reduce(const uint8_t *const *codes, const float *const *scales, int nranks,
+              size_t n, int block, void *out, lpcoll_dtype dtype, void *stream)
+{
+    if (bad_dtype(dtype) || nranks < 1 || nranks > LPCOLL_MAX_RANKS)
+        return LPCOLL_ERR_ARG;
+    if (block != LPCOLL_BLOCK)
+        return LPCOLL_ERR_UNSUPPORTED;
+    if (n == 0)
+        return LPCOLL_OK;
+    int st = first_error({check_rank_array(codes, nranks),
+                          check_rank_array(scales, nranks), check_ptr(out)});
+    if (st != LPCOLL_OK)
+        return st;
+    ReduceParams p = {};
+    for (int r = 0; r < nranks; ++r) {
+        p.codes[r] = codes[r];
+        p.scales[r] = scales[r];
+    }
+    return finish(launch_reduce(p, nranks, n, out, dtype,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+int dda_flat_sim(const void *const *in, void *const *out, int nranks, size_t n,
+                 lpcoll_dtype dtype, int block, uint8_t *const *wire_codes,
+                 float *const *wire_scales, void *stream)
+{
+    return dda_common(in, out, nranks, n, dtype, block, wire_codes, wire_scales,
+                      nullptr, nullptr, false, stream);
+}
+
+int dda_tree_sim(const void *const *in, void *const *out, int nranks, size_t n,
+                 lpcoll_dtype dtype, int block, uint8_t *const *wire_codes,
+                 float *const *wire_scales, uint8_t *shard_codes,
+                 float *shard_scales, void *stream)
+{
+    return dda_common(in, out, nranks, n, dtype, block, wire_codes, wire_scales,
+                      shard_codes, shard_scales, true, stream);
+}
+
+const char *lpcoll_status_string(int status)
+{
+    switch (status) {
+    case LPCOLL_OK: return "LPCOLL_OK";
+    case LPCOLL_ERR_ARG: return "LPCOLL_ERR_ARG: invalid argument or NULL pointer";
+    case LPCOLL_ERR_ALIGN: return "LPCOLL_ERR_ALIGN: device pointer not 16-byte aligned";
+    case LPCOLL_ERR_UNSUPPORTED: return "LPCOLL_ERR_UNSUPPORTED: unsupported block size";
+    case LPCOLL_ERR_RANK: return "LPCOLL_ERR_RANK: NULL pointer in a per-rank array";
+    case LPCOLL_ERR_CUDA: return "LPCOLL_ERR_CUDA: kernel launch failed";
+    default: return "LPCOLL: unknown status";
+    }
+}
+
+int lpcoll_last_cuda_error(void) { return g_last_cuda_error; }
+
+int lpcoll_version(void) { return 100; }
+
+}  // extern "C"

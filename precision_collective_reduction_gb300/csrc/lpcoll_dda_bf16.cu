@@ -1,0 +1,10 @@
+// BF16 instantiations of the fused DDA allreduce kernels (N = 1..16).
+#include "lpcoll_dda.cuh"
+
+namespace lpc {
+cudaError_t launch_dda_bf16(const DdaParams &p, int nranks, size_t n, int mode,
+                            cudaStream_t stream)
+{
+    return launch_dda<LPCOLL_BF16>(p, nranks, n, mode, stream);
+}
+}  // namespace lpc

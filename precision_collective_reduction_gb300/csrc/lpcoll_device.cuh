@@ -1,0 +1,340 @@
+// lpcoll_device.cuh -- device building blocks shared by the kernels of
+// liblpcoll: 16-byte vector access, BF16 widening / narrowing, block absmax,
+// the per-block FP8 scale, and E4M3 packing with the hardware cvt.
+//
+// Work decomposition used by every kernel: a "unit" is one warp-width of
+// 16-byte vectors of one rank's message, i.e. 32 x kVec elements: one
+// 128-element block for FP32 (4 elements per lane), two blocks for BF16
+// (8 elements per lane, one block per half-warp). A block's absmax is
+// therefore a shuffle reduction inside a group of kGroup lanes (32 or 16).
+//
+// All floating-point steps are single IEEE binary32 operations rounded to
+// nearest even, written with the __f*_rn intrinsics so that the compiler can
+// neither contract them into FMAs nor swap a division for a reciprocal.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lpcoll.h"
+
+namespace lpc {
+
+constexpr int kBlock = LPCOLL_BLOCK;  // elements per scale block
+constexpr float kE4M3Max = 448.0f;    // largest finite E4M3 value
+constexpr int kThreads = 256;         // threads per CTA of every kernel
+constexpr int kWarpsPerCta = kThreads / 32;
+
+enum Mode { kExact = 0, kFlat = 1, kTree = 2 };
+
+// Element format traits: elements per 16-byte vector and lanes per block.
+template <int DT> struct Fmt;
+template <> struct Fmt<LPCOLL_F32> {
+    static constexpr int kVec = 4;
+    static constexpr int kGroup = 32;
+};
+template <> struct Fmt<LPCOLL_BF16> {
+    static constexpr int kVec = 8;
+    static constexpr int kGroup = 16;
+};
+
+// Per-rank pointers of a fused allreduce launch (passed by value).
+struct DdaParams {
+    const void *in[LPCOLL_MAX_RANKS];
+    void *out[LPCOLL_MAX_RANKS];
+    uint8_t *codes[LPCOLL_MAX_RANKS];
+    float *scales[LPCOLL_MAX_RANKS];
+    uint8_t *shard_codes;
+    float *shard_scales;
+};
+
+// Per-rank payload pointers of lp_reduce.
+struct ReduceParams {
+    const uint8_t *codes[LPCOLL_MAX_RANKS];
+    const float *scales[LPCOLL_MAX_RANKS];
+};
+
+// ---------------------------------------------------------------------------
+// Memory access. Messages are streamed once: loads and stores use the
+// evict-first cache policy. A lane holding fewer than kVec valid elements
+// (only in the last, ragged unit) falls back to element accesses; missing
+// elements read as +0, which leaves a block maximum unchanged.
+// ---------------------------------------------------------------------------
+
+template <int DT>
+__device__ __forceinline__ uint4 load_vec(const void *base, size_t e0, int cnt)
+{
+    constexpr int V = Fmt<DT>::kVec;
+    constexpr int ES = 16 / V;  // element size in bytes
+    const char *p = static_cast<const char *>(base) + e0 * ES;
+    if (cnt == V)
+        return __ldcs(reinterpret_cast<const uint4 *>(p));
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (DT == LPCOLL_F32) {
+        const uint32_t *q = reinterpret_cast<const uint32_t *>(p);
+        for (int j = 0; j < cnt; ++j)
+            w[j] = q[j];
+    } else {
+        const uint16_t *q = reinterpret_cast<const uint16_t *>(p);
+        for (int j = 0; j < cnt; ++j)
+            w[j >> 1] |= static_cast<uint32_t>(q[j]) << (16 * (j & 1));
+    }
+    v.x = w[0];
+    v.y = w[1];
+    v.z = w[2];
+    v.w = w[3];
+    return v;
+}
+
+template <int DT>
+__device__ __forceinline__ void store_vec(void *base, size_t e0, int cnt, uint4 v)
+{
+    constexpr int V = Fmt<DT>::kVec;
+    constexpr int ES = 16 / V;
+    char *p = static_cast<char *>(base) + e0 * ES;
+    if (cnt == V) {
+        __stcs(reinterpret_cast<uint4 *>(p), v);
+        return;
+    }
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (DT == LPCOLL_F32) {
+        uint32_t *q = reinterpret_cast<uint32_t *>(p);
+        for (int j = 0; j < cnt; ++j)
+            q[j] = w[j];
+    } else {
+        uint16_t *q = reinterpret_cast<uint16_t *>(p);
+        for (int j = 0; j < cnt; ++j)
+            q[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+    }
+}
+
+// kVec codes of one lane, packed little-endian (element e0 in the low byte).
+template <int DT> struct Codes;
+template <> struct Codes<LPCOLL_F32> {
+    uint32_t w;
+};
+template <> struct Codes<LPCOLL_BF16> {
+    uint2 w;
+};
+
+__device__ __forceinline__ void store_codes(uint8_t *base, size_t e0, int cnt,
+                                            Codes<LPCOLL_F32> c)
+{
+    if (cnt == 4) {
+        __stcs(reinterpret_cast<unsigned int *>(base + e0), c.w);
+        return;
+    }
+    for (int j = 0; j < cnt; ++j)
+        base[e0 + j] = static_cast<uint8_t>(c.w >> (8 * j));
+}
+
+__device__ __forceinline__ void store_codes(uint8_t *base, size_t e0, int cnt,
+                                            Codes<LPCOLL_BF16> c)
+{
+    if (cnt == 8) {
+        __stcs(reinterpret_cast<uint2 *>(base + e0), c.w);
+        return;
+    }
+    for (int j = 0; j < cnt; ++j) {
+        uint32_t word = j < 4 ? c.w.x : c.w.y;
+        base[e0 + j] = static_cast<uint8_t>(word >> (8 * (j & 3)));
+    }
+}
+
+__device__ __forceinline__ Codes<LPCOLL_F32> load_codes_f32(const uint8_t *base,
+                                                           size_t e0, int cnt)
+{
+    Codes<LPCOLL_F32> c;
+    if (cnt == 4) {
+        c.w = __ldcs(reinterpret_cast<const unsigned int *>(base + e0));
+        return c;
+    }
+    c.w = 0u;
+    for (int j = 0; j < cnt; ++j)
+        c.w |= static_cast<uint32_t>(base[e0 + j]) << (8 * j);
+    return c;
+}
+
+__device__ __forceinline__ Codes<LPCOLL_BF16> load_codes_bf16(const uint8_t *base,
+                                                             size_t e0, int cnt)
+{
+    Codes<LPCOLL_BF16> c;
+    if (cnt == 8) {
+        c.w = __ldcs(reinterpret_cast<const uint2 *>(base + e0));
+        return c;
+    }
+    c.w = make_uint2(0u, 0u);
+    for (int j = 0; j < cnt; ++j) {
+        uint32_t b = static_cast<uint32_t>(base[e0 + j]) << (8 * (j & 3));
+        if (j < 4)
+            c.w.x |= b;
+        else
+            c.w.y |= b;
+    }
+    return c;
+}
+
+template <int DT>
+__device__ __forceinline__ Codes<DT> load_codes(const uint8_t *base, size_t e0, int cnt);
+template <>
+__device__ __forceinline__ Codes<LPCOLL_F32> load_codes<LPCOLL_F32>(const uint8_t *base,
+                                                                   size_t e0, int cnt)
+{
+    return load_codes_f32(base, e0, cnt);
+}
+template <>
+__device__ __forceinline__ Codes<LPCOLL_BF16> load_codes<LPCOLL_BF16>(const uint8_t *base,
+                                                                     size_t e0, int cnt)
+{
+    return load_codes_bf16(base, e0, cnt);
+}
+
+// ---------------------------------------------------------------------------
+// Element formats
+// ---------------------------------------------------------------------------
+
+// 16 bytes -> kVec floats (FP32: reinterpretation; BF16: exact shift).
+template <int DT>
+__device__ __forceinline__ void widen(uint4 v, float (&x)[Fmt<DT>::kVec])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (DT == LPCOLL_F32) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            x[j] = __uint_as_float(w[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            x[2 * j] = __uint_as_float(w[j] << 16);
+            x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    }
+}
+
+// kVec floats -> 16 bytes (BF16: round to nearest even).
+template <int DT>
+__device__ __forceinline__ uint4 narrow(const float (&x)[Fmt<DT>::kVec])
+{
+    uint32_t w[4];
+    if constexpr (DT == LPCOLL_F32) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            w[j] = __float_as_uint(x[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * j], x[2 * j + 1]);
+            w[j] = *reinterpret_cast<uint32_t *>(&h);
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ---------------------------------------------------------------------------
+// FP8 block quantization
+// ---------------------------------------------------------------------------
+
+// Largest |x| over the kGroup lanes holding one block (max is exact, so the
+// shuffle order does not matter).
+template <int G>
+__device__ __forceinline__ float group_max(float v)
+{
+#pragma unroll
+    for (int m = G / 2; m >= 1; m >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+    return v;
+}
+
+// Block scale s = a/448 and element multiplier inv = 448/a, each one IEEE
+// division. If 448/a overflows, the block is degenerate: s = inv = 0, which
+// turns every element into a signed zero code.
+__device__ __forceinline__ void block_scale(float amax, float &s, float &inv)
+{
+    inv = __fdiv_rn(kE4M3Max, amax);
+    if (isinf(inv)) {
+        inv = 0.0f;
+        s = 0.0f;
+    } else {
+        s = __fdiv_rn(amax, kE4M3Max);
+    }
+}
+
+// Two floats -> two E4M3 codes (a in the low byte), RNE, saturating.
+__device__ __forceinline__ uint32_t enc2(float a, float b)
+{
+    return static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Two E4M3 codes (low byte first) -> two exact floats (via FP16, exact).
+__device__ __forceinline__ float2 dec2(uint32_t c2)
+{
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+        static_cast<__nv_fp8x2_storage_t>(c2 & 0xFFFFu), __NV_E4M3);
+    return __half22float2(__half2(h));
+}
+
+// Quantize the kVec values of this lane (block scale from its group):
+// returns the packed codes and writes s.
+template <int DT>
+__device__ __forceinline__ Codes<DT> quantize_lane(const float (&x)[Fmt<DT>::kVec],
+                                                   float &s)
+{
+    constexpr int V = Fmt<DT>::kVec;
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+        amax = fmaxf(amax, fabsf(x[j]));
+    amax = group_max<Fmt<DT>::kGroup>(amax);
+    float inv;
+    block_scale(amax, s, inv);
+    uint32_t c2[V / 2];
+#pragma unroll
+    for (int j = 0; j < V / 2; ++j)
+        c2[j] = enc2(__fmul_rn(x[2 * j], inv), __fmul_rn(x[2 * j + 1], inv));
+    Codes<DT> c;
+    if constexpr (DT == LPCOLL_F32) {
+        c.w = c2[0] | (c2[1] << 16);
+    } else {
+        c.w = make_uint2(c2[0] | (c2[1] << 16), c2[2] | (c2[3] << 16));
+    }
+    return c;
+}
+
+// Dequantize this lane's codes with scale s: v = fl(e4m3 * s).
+template <int DT>
+__device__ __forceinline__ void dequantize_lane(Codes<DT> c, float s,
+                                                float (&v)[Fmt<DT>::kVec])
+{
+    constexpr int V = Fmt<DT>::kVec;
+    uint32_t words[V / 4];
+    if constexpr (DT == LPCOLL_F32) {
+        words[0] = c.w;
+    } else {
+        words[0] = c.w.x;
+        words[1] = c.w.y;
+    }
+#pragma unroll
+    for (int k = 0; k < V / 4; ++k) {
+        float2 lo = dec2(words[k]);
+        float2 hi = dec2(words[k] >> 16);
+        v[4 * k + 0] = __fmul_rn(lo.x, s);
+        v[4 * k + 1] = __fmul_rn(lo.y, s);
+        v[4 * k + 2] = __fmul_rn(hi.x, s);
+        v[4 * k + 3] = __fmul_rn(hi.y, s);
+    }
+}
+
+// Number of valid elements of a lane whose first element is e0.
+template <int DT>
+__device__ __forceinline__ int lane_count(size_t n, size_t e0)
+{
+    constexpr int V = Fmt<DT>::kVec;
+    return e0 >= n ? 0 : (n - e0 >= (size_t)V ? V : static_cast<int>(n - e0));
+}
+
+}  // namespace lpc

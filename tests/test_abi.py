@@ -1,0 +1,127 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/lpcoll.h declares, and rejects bad arguments on the host before any
+launch (every call below fails validation, so nothing reaches CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import precision_collective_reduction_gb300 as pcr
+from precision_collective_reduction_gb300 import _binding as B
+from precision_collective_reduction_gb300 import build as lib_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "lpcoll.h")
+OK, ARG, ALIGN, UNSUP, RANK = 0, 1, 2, 3, 4
+A = 0x10000  # an aligned fake device address: never dereferenced in these calls
+
+
+@pytest.fixture(scope="module")
+def L():
+    lib_build.build()
+    return pcr.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)) -
+                  {"if", "defined"})
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert {"lp_quantize", "lp_dequantize", "lp_reduce", "dda_flat_sim",
+            "dda_tree_sim", "lpcoll_status_string"} <= set(names)
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for st, name in B.STATUS.items():
+        assert L.lpcoll_status_string(st).decode().startswith(name)
+    assert b"unknown" in L.lpcoll_status_string(99)
+    assert L.lpcoll_version() == 100
+    assert L.lpcoll_last_cuda_error() == 0
+
+
+def arr(*ptrs):
+    return B.ptr_array(ptrs)
+
+
+def test_quantize_validation(L):
+    assert L.lp_quantize(A, 7, 10, 128, A, A, None) == ARG
+    assert L.lp_quantize(A, 0, 10, 64, A, A, None) == UNSUP
+    assert L.lp_quantize(A, 0, 10, 0, A, A, None) == UNSUP
+    assert L.lp_quantize(None, 0, 0, 128, None, None, None) == OK  # n == 0
+    assert L.lp_quantize(None, 0, 10, 128, A, A, None) == ARG
+    assert L.lp_quantize(A, 1, 10, 128, None, A, None) == ARG
+    assert L.lp_quantize(A + 4, 0, 10, 128, A, A, None) == ALIGN
+    assert L.lp_quantize(A, 0, 10, 128, A, A + 8, None) == ALIGN
+    # NULL is reported before misalignment
+    assert L.lp_quantize(A + 4, 0, 10, 128, None, A, None) == ARG
+
+
+def test_dequantize_validation(L):
+    assert L.lp_dequantize(A, A, 10, 128, A, 2, None) == ARG
+    assert L.lp_dequantize(A, A, 10, 256, A, 0, None) == UNSUP
+    assert L.lp_dequantize(A, A, 0, 128, None, 0, None) == OK
+    assert L.lp_dequantize(A, None, 10, 128, A, 0, None) == ARG
+    assert L.lp_dequantize(A, A, 10, 128, A + 2, 1, None) == ALIGN
+
+
+def test_reduce_validation(L):
+    two = arr(A, A)
+    assert L.lp_reduce(two, two, 0, 10, 128, A, 0, None) == ARG
+    assert L.lp_reduce(two, two, 17, 10, 128, A, 0, None) == ARG
+    assert L.lp_reduce(two, two, 2, 10, 32, A, 0, None) == UNSUP
+    assert L.lp_reduce(two, two, 2, 0, 128, None, 0, None) == OK
+    assert L.lp_reduce(None, two, 2, 10, 128, A, 0, None) == ARG
+    assert L.lp_reduce(arr(A, None), two, 2, 10, 128, A, 0, None) == RANK
+    assert L.lp_reduce(two, arr(A, A + 4), 2, 10, 128, A, 0, None) == ALIGN
+    assert L.lp_reduce(two, two, 2, 10, 128, None, 0, None) == ARG
+
+
+@pytest.mark.parametrize("fn", ["dda_flat_sim", "dda_tree_sim"])
+def test_allreduce_validation(L, fn):
+    f = getattr(L, fn)
+    tree = fn == "dda_tree_sim"
+
+    def call(ins, outs, N, n, dt, block, wc, ws, sc=A, ss=A):
+        if tree:
+            return f(ins, outs, N, n, dt, block, wc, ws, sc, ss, None)
+        return f(ins, outs, N, n, dt, block, wc, ws, None)
+
+    two = arr(A, A)
+    assert call(two, two, 2, 10, 5, 128, two, two) == ARG          # dtype
+    assert call(two, two, 0, 10, 0, 128, two, two) == ARG          # N < 1
+    assert call(two, two, 17, 10, 0, 128, two, two) == ARG         # N > 16
+    assert call(two, two, 2, 10, 0, 64, two, two) == UNSUP         # block
+    assert call(None, None, 2, 0, 0, 128, None, None) == OK        # n == 0
+    assert call(None, two, 2, 10, 0, 0, None, None) == ARG
+    assert call(arr(A, None), two, 2, 10, 0, 0, None, None) == RANK
+    assert call(two, arr(None, A), 2, 10, 1, 0, None, None) == RANK
+    assert call(two, two, 2, 10, 0, 128, None, two) == ARG         # LP needs wires
+    assert call(two, two, 2, 10, 0, 128, two, arr(A, None)) == RANK
+    assert call(arr(A, A + 8), two, 2, 10, 0, 0, None, None) == ALIGN
+    assert call(two, two, 2, 10, 0, 128, arr(A + 1, A), two) == ALIGN
+    # a NULL anywhere wins over a misaligned pointer anywhere
+    assert call(arr(A + 8, A), arr(A, None), 2, 10, 0, 0, None, None) == RANK
+    if tree:
+        assert call(two, two, 2, 10, 0, 128, two, two, sc=None) == ARG
+        assert call(two, two, 2, 10, 0, 128, two, two, ss=A + 4) == ALIGN
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(RuntimeError, match="not found"):
+        B.lib()
+
+
+def test_library_is_built_for_sm103a():
+    lib_build.build()
+    assert "arch=compute_103a,code=sm_103a" in " ".join(lib_build.NVCC_FLAGS)
+    assert os.path.getsize(lib_build.LIB) > 0
+    ctypes.CDLL(lib_build.LIB)
