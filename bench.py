@@ -83,6 +83,22 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x, dist, device):
+    """Largest value of x over all ranks (x itself when not distributed)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(bytes_per_step, steps, world, max_ms):
+    """Whole-job throughput: the bytes every rank processed over the slowest
+    rank's time."""
+    return bytes_per_step * steps * world / (max_ms / 1e3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -372,12 +388,9 @@ def run_ours(args):
     total_ms, per_kernel, (t0, t1) = timed_steps(torch, bufs, w, stream, args.steps,
                                                  args.warmup, dist, clocks)
     clock_info = clocks.summary(t0, t1)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, "cuda")
     sbytes = step_bytes(w)
-    value = sbytes * args.steps * world / (total_ms / 1e3) / 1e9
+    value = whole_job_gbps(sbytes, args.steps, world, total_ms)
 
     peak, peak_kind = measured_peaks()
     avg = {a: statistics.fmean(v) for a, v in per_kernel.items()}
@@ -404,13 +417,10 @@ def run_ours(args):
                     for _ in range(w.nranks)] for a in w.algos}
     e2e_n = min(args.steps, E2E_MAX_STEPS)
     e2e_ms = e2e_steps(torch, bufs, w, stream, e2e_n, host_in, host_out)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
     h2d = sum(x.nbytes for x in host)
     d2h = sum(h.numel() * h.element_size() for a in w.algos for h in host_out[a])
-    e2e = {"value": round(sbytes * e2e_n * world / (e2e_ms / 1e3) / 1e9, 2),
+    e2e = {"value": round(whole_job_gbps(sbytes, e2e_n, world, e2e_ms), 2),
            "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": round(e2e_ms / e2e_n, 3), "steps": e2e_n}
     del host_in, host_out, bufs
@@ -488,10 +498,10 @@ def main():
                     help="with --profile-case: elements per rank (default: full)")
     ap.add_argument("--algo", choices=["flat", "tree"], default=None)
     args = ap.parse_args()
-    if args.warmup < 3:
-        ap.error("--warmup must be at least 3")
     if args.profile_case:
         return run_profile_case(args)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -1,0 +1,60 @@
+"""Host-side logic that needs no GPU: algorithm choice of the allreduce
+facade, benchmark byte accounting, and the workload recipes."""
+import numpy as np
+import pytest
+
+import bench
+from precision_collective_reduction_gb300 import allreduce as AR
+from precision_collective_reduction_gb300 import workloads as W
+
+MiB = 1 << 20
+
+
+def test_low_precision_off_by_default():
+    assert AR.choose(64 * MiB, env={}) == ("flat", 0)
+
+
+def test_env_switch_and_threshold():
+    env = {AR.LP_ENV: "1"}
+    assert AR.choose(16 * MiB, env=env) == ("flat", 128)       # at the threshold
+    assert AR.choose(16 * MiB - 1, env=env) == ("flat", 0)     # below it
+    env[AR.LP_MIN_BYTES_ENV] = "1024"
+    assert AR.choose(4096, env=env) == ("flat", 128)
+
+
+def test_argument_overrides_env():
+    assert AR.choose(32 * MiB, low_precision=True, env={}) == ("flat", 128)
+    assert AR.choose(32 * MiB, low_precision=False, env={AR.LP_ENV: "1"}) == ("flat", 0)
+
+
+def test_algo_selection():
+    assert AR.choose(1024, algo="tree", env={}) == ("tree", 0)
+    env = {AR.TREE_MIN_BYTES_ENV: str(MiB)}
+    assert AR.choose(MiB, env=env)[0] == "tree"
+    assert AR.choose(MiB - 1, env=env)[0] == "flat"
+    with pytest.raises(ValueError):
+        AR.choose(1, algo="ring", env={})
+
+
+def test_algorithmic_bytes_match_the_formulas():
+    # N n (2 s + q) for flat, plus n q for the tree's shard wire, with
+    # q = 1 + 4/128 bytes per element of FP8 payload
+    w = W.LP_GRAD_N8_256MB_F32
+    assert bench.bytes_alg(8, w.n, 4, 128, "flat") == 4_848_615_424
+    assert bench.bytes_alg(8, w.n, 4, 128, "tree") == 4_917_821_440
+    assert bench.bytes_alg(2, 1 << 20, 4, 128, "flat") == 18_939_904
+    assert bench.bytes_alg(8, 32 * 8192, 2, 0, "flat") == 8_388_608
+    assert bench.bytes_alg(8, 8 * MiB, 2, 128, "flat") == 337_641_472
+    assert bench.bytes_alg(8, 32 * MiB, 2, 128, "tree") == 1_385_168_896
+
+
+def test_workload_recipes():
+    w = W.LP_GRAD_N8_256MB_F32
+    x = W.draw(w, 0, n=128 * 1000)
+    big = np.abs(x.reshape(-1, 128)).max(axis=1) > 0.05
+    assert 3 <= big.sum() <= 30          # about 1% of blocks scaled by 1e3
+    d = W.draw(W.DECODE_EXACT_FLAT_N8_BF16, 0)
+    assert d.dtype == np.uint16 and d.size == 32 * 8192
+    a = W.draw(W.LP_FLAT_N2_1M_F32, 1, n=1000)
+    assert np.array_equal(a, W.draw(W.LP_FLAT_N2_1M_F32, 1, n=1000))   # seeded
+    assert not np.array_equal(a, W.draw(W.LP_FLAT_N2_1M_F32, 0, n=1000))
