@@ -133,6 +133,35 @@ int dda_tree_sim(const void *const *in, void *const *out, int nranks,
                  uint8_t *const *wire_codes, float *const *wire_scales,
                  uint8_t *shard_codes, float *shard_scales, void *stream);
 
+/* dda_flat_sim with block = 128 for callers that cannot allocate device
+ * memory. The pages have no counterpart: this exists for users of the
+ * library, not for the method. Some callers cannot provide the wire buffers
+ * that dda_flat_sim needs as scratch, for instance a plugin running inside a
+ * host framework that owns all device memory, or a latency-critical loop
+ * that must never call cudaMalloc (which can synchronize the device). This
+ * call keeps every rank's FP8 wire payload in a fixed array inside the
+ * library's device image and allocates nothing; it gives the same outputs as
+ * dda_flat_sim with block = 128.
+ *   in, out, nranks, n, dtype, stream   as dda_flat_sim; the caller still
+ *                                       owns and passes inputs and outputs
+ *   limit    nranks * ceil(n / 256) * 256 <= LPCOLL_NOALLOC_MAX_ELEMS
+ *            (64 Mi elements over all ranks, e.g. 8 ranks of 8 Mi elements,
+ *            a 16 MiB BF16 message); larger calls return LPCOLL_ERR_ARG and
+ *            launch nothing.
+ *   memory   every GPU on which the library's kernels are loaded holds the
+ *            array (about 66 MiB) until the process exits. The first call
+ *            with a device current looks up the array's device address on
+ *            that device (cudaGetSymbolAddress); make that first call before
+ *            any stream capture.
+ *   sharing  all calls share the one array and it keeps the last call's
+ *            wire payload (nothing in it needs to start at zero). Calls that
+ *            overlap on the GPU (different streams, or threads) race on it:
+ *            their outputs stay correct, since no kernel reads the array
+ *            back, but its contents are then undefined.                    */
+#define LPCOLL_NOALLOC_MAX_ELEMS (64u * 1024u * 1024u)
+int dda_flat_sim_noalloc(const void *const *in, void *const *out, int nranks,
+                         size_t n, lpcoll_dtype dtype, void *stream);
+
 /* Static, NUL-terminated name of a status code (never NULL). */
 const char *lpcoll_status_string(int status);
 
