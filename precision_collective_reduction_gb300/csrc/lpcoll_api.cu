@@ -38,7 +38,7 @@ struct OccHash {
 };
 
 std::mutex g_occ_mutex;
-std::unordered_map<OccKey, int, OccHash> g_wave;  // CTAs in one full wave
+std::unordered_map<OccKey, int, OccHash> g_wave;  // CTAs of one launch wave
 
 int full_wave(const void *kernel)
 {
@@ -52,6 +52,8 @@ int full_wave(const void *kernel)
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+    if (per_sm > kCtasPerSm)
+        per_sm = kCtasPerSm;
     int wave = sms * per_sm;
     if (wave < 1)
         wave = 1;

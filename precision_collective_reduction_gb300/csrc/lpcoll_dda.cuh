@@ -16,8 +16,9 @@
 // Every element is read before any output of its unit is written, so an
 // output may alias its input.
 //
-// The warps stride over units (grid-stride loop); the grid is at most one
-// full wave of CTAs, so blocks of the same rank stream through HBM in order.
+// The warps stride over units (grid-stride loop); the grid is at most
+// kCtasPerSm CTAs per SM, all resident at once, so the units of every rank
+// stream through HBM in order.
 #pragma once
 
 #include "lpcoll_device.cuh"
@@ -109,7 +110,7 @@ inline void unit_counts(size_t n, size_t &full, size_t &total)
 }
 
 // CTAs for a launch covering `units` warp-units: enough for every unit, at
-// most one full wave (resident CTAs per SM x SMs).
+// most min(resident CTAs per SM, kCtasPerSm) x SMs.
 int wave_ctas(const void *kernel, size_t units);
 
 template <int N, int DT, int MODE>
