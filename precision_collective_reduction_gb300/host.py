@@ -7,9 +7,9 @@ whose boundaries are multiples of 128 elements with results identical to one
 launch over the whole message. ``HostAllreduce`` streams the chunks through a
 ring of device slots on three CUDA streams:
 
-    h2d stream:     copy chunk k of every rank's input into slot k % S
+    h2d streams:    copy chunk k of every rank's input into slot k % S
     compute stream: run the requested allreduce(s) on slot k % S
-    d2h stream:     copy chunk k of every result back to host memory
+    d2h streams:    copy chunk k of every result back to host memory
 
 Events order the three stages of one chunk and keep a slot from being
 refilled before its results have left the GPU, so copies in both directions
@@ -25,7 +25,7 @@ TORCH_DT = {B.F32: torch.float32, B.BF16: torch.bfloat16}
 
 
 class _Slot:
-    def __init__(self, nranks, chunk, dtype, block, algos, device):
+    def __init__(self, nranks, chunk, dtype, block, algos, device, ncopy):
         tdt = TORCH_DT[dtype]
         nb = B.nblocks(chunk)
         self.ins = [torch.empty(chunk, dtype=tdt, device=device) for _ in range(nranks)]
@@ -46,9 +46,9 @@ class _Slot:
             self.p_sc = self.p_ss = 0
         self.p_in = [t.data_ptr() for t in self.ins]
         self.p_out = {a: [t.data_ptr() for t in v] for a, v in self.outs.items()}
-        self.h2d_done = torch.cuda.Event()
+        self.h2d_done = [torch.cuda.Event() for _ in range(ncopy)]
         self.compute_done = torch.cuda.Event()
-        self.d2h_done = torch.cuda.Event()
+        self.d2h_done = [torch.cuda.Event() for _ in range(ncopy)]
         self.used = False
 
 
@@ -58,10 +58,12 @@ class HostAllreduce:
     algos: which allreduces to run on every chunk, "flat" and/or "tree"; each
     writes its own set of N host outputs. chunk: elements per chunk (rounded
     up to a multiple of 128). slots: device buffers in flight (>= 2).
+    copy_streams: streams per copy direction; rank r's copies go on stream
+    r % copy_streams, so several copy engines can work at once.
     """
 
     def __init__(self, nranks, n, dtype, block=B.BLOCK, algos=("flat",),
-                 chunk=1 << 22, slots=3, device="cuda"):
+                 chunk=1 << 22, slots=3, copy_streams=1, device="cuda"):
         if block not in (0, B.BLOCK):
             raise ValueError("block must be 0 or %d" % B.BLOCK)
         if slots < 2:
@@ -71,11 +73,13 @@ class HostAllreduce:
         chunk = max(B.BLOCK, (min(chunk, max(n, 1)) + B.BLOCK - 1) // B.BLOCK * B.BLOCK)
         self.chunk = chunk
         self.device = torch.device(device)
-        self.slots = [_Slot(nranks, chunk, dtype, block, self.algos, self.device)
-                      for _ in range(min(slots, max(1, -(-n // chunk))) or 1)]
-        self.h2d = torch.cuda.Stream(self.device)
+        self.ncopy = max(1, min(copy_streams, nranks))
+        nslots = max(1, min(slots, -(-n // chunk)))
+        self.slots = [_Slot(nranks, chunk, dtype, block, self.algos, self.device,
+                            self.ncopy) for _ in range(nslots)]
+        self.h2d = [torch.cuda.Stream(self.device) for _ in range(self.ncopy)]
         self.compute = torch.cuda.Stream(self.device)
-        self.d2h = torch.cuda.Stream(self.device)
+        self.d2h = [torch.cuda.Stream(self.device) for _ in range(self.ncopy)]
 
     def chunks(self):
         for k, lo in enumerate(range(0, self.n, self.chunk)):
@@ -93,42 +97,51 @@ class HostAllreduce:
 
     def run(self, host_ins, host_outs):
         """host_ins: N host tensors of n elements; host_outs: {algo: N host
-        tensors}. Enqueues everything and returns; call ``synchronize()`` (or
-        wait on ``self.d2h``) before reading host_outs."""
+        tensors}. Enqueues everything and returns; call ``synchronize()``
+        before reading host_outs."""
         if len(host_ins) != self.nranks:
             raise ValueError("one input per rank")
         S = len(self.slots)
+        C = self.ncopy
         for k, lo, hi in self.chunks():
             m = hi - lo
             slot = self.slots[k % S]
-            with torch.cuda.stream(self.h2d):
-                if slot.used:
-                    self.h2d.wait_event(slot.d2h_done)
-                for t, h in zip(slot.ins, host_ins):
-                    t[:m].copy_(h[lo:hi], non_blocking=True)
-                slot.h2d_done.record(self.h2d)
-            self.compute.wait_event(slot.h2d_done)
+            for i, st in enumerate(self.h2d):
+                with torch.cuda.stream(st):
+                    if slot.used:
+                        for ev in slot.d2h_done:
+                            st.wait_event(ev)
+                    for r in range(i, self.nranks, C):
+                        slot.ins[r][:m].copy_(host_ins[r][lo:hi], non_blocking=True)
+                    slot.h2d_done[i].record(st)
+            for ev in slot.h2d_done:
+                self.compute.wait_event(ev)
             for a in self.algos:
                 self._launch(slot, a, m)
             slot.compute_done.record(self.compute)
-            with torch.cuda.stream(self.d2h):
-                self.d2h.wait_event(slot.compute_done)
-                for a in self.algos:
-                    for t, h in zip(slot.outs[a], host_outs[a]):
-                        h[lo:hi].copy_(t[:m], non_blocking=True)
-                slot.d2h_done.record(self.d2h)
+            for i, st in enumerate(self.d2h):
+                with torch.cuda.stream(st):
+                    st.wait_event(slot.compute_done)
+                    for a in self.algos:
+                        for r in range(i, self.nranks, C):
+                            host_outs[a][r][lo:hi].copy_(slot.outs[a][r][:m],
+                                                         non_blocking=True)
+                    slot.d2h_done[i].record(st)
             slot.used = True
 
     def synchronize(self):
-        self.d2h.synchronize()
+        for st in self.d2h:
+            st.synchronize()
 
     def start_after(self, stream):
         """Make the next run's first copies wait for work queued on stream."""
-        self.h2d.wait_stream(stream)
+        for st in self.h2d:
+            st.wait_stream(stream)
 
     def finish_before(self, stream):
         """Make work queued on stream afterwards wait for the last results."""
-        stream.wait_stream(self.d2h)
+        for st in self.d2h:
+            stream.wait_stream(st)
 
     def kernel_launches_per_run(self):
         return len(self.algos) * len(list(self.chunks()))
