@@ -47,6 +47,10 @@ def _load(path):
                            ctypes.c_int, pp, pp]
     L.orc_tree.argtypes = [pp, pp, ctypes.c_int, c_sz, ctypes.c_int,
                            ctypes.c_int, pp, pp, vp, vp]
+    for f in ("orc_reduce_scatter", "orc_all_gather", "orc_all_to_all"):
+        getattr(L, f).argtypes = [pp, pp, ctypes.c_int, c_sz, ctypes.c_int,
+                                  ctypes.c_int, pp, pp]
+        getattr(L, f).restype = ctypes.c_int
     L.orc_shard_len.argtypes = [c_sz, ctypes.c_int, ctypes.c_int]
     L.orc_shard_len.restype = c_sz
     for f in ("orc_quantize", "orc_dequantize", "orc_reduce", "orc_flat",
@@ -229,6 +233,75 @@ def tree(inputs, block=BLOCK):
         sc = sc[:n]
         ss = ss[:nblocks(n, block)]
     return outs, wc, ws, sc, ss
+
+
+def reduce_scatter(inputs, block=BLOCK):
+    """LP ReduceScatter. Returns (outputs, wire_codes, wire_scales); output r
+    holds shard r (length min(L, n - r L), L = shard_len(n, N, block))."""
+    inputs = [np.ascontiguousarray(x) for x in inputs]
+    nranks = len(inputs)
+    n = inputs[0].size
+    per = shard_len(n, nranks, block) if n else 0
+    lens = [max(0, min(per, n - r * per)) for r in range(nranks)]
+    outs = [np.zeros(max(k, 1), dtype=inputs[0].dtype) for k in lens]
+    wc, ws = _wires(nranks, n, block)
+    null = (ctypes.c_void_p * nranks)()
+    _check(lib().orc_reduce_scatter(_ptrs(inputs), _ptrs(outs), nranks, n,
+                                    _dtype_code(inputs[0]), block,
+                                    _ptrs(wc) if wc else null,
+                                    _ptrs(ws) if ws else null), "reduce_scatter")
+    outs = [o[:k] for o, k in zip(outs, lens)]
+    if wc is not None:
+        wc = [c[:n] for c in wc]
+        ws = [s[:nblocks(n, block)] for s in ws]
+    return outs, wc, ws
+
+
+def all_gather(inputs, block=BLOCK):
+    """LP AllGather of N contributions of m elements. Returns (outputs of
+    N*m elements, wire_codes, wire_scales)."""
+    inputs = [np.ascontiguousarray(x) for x in inputs]
+    nranks = len(inputs)
+    m = inputs[0].size
+    outs = [np.zeros(max(nranks * m, 1), dtype=inputs[0].dtype) for _ in range(nranks)]
+    wc, ws = _wires(nranks, m, block)
+    null = (ctypes.c_void_p * nranks)()
+    _check(lib().orc_all_gather(_ptrs(inputs), _ptrs(outs), nranks, m,
+                                _dtype_code(inputs[0]), block,
+                                _ptrs(wc) if wc else null,
+                                _ptrs(ws) if ws else null), "all_gather")
+    outs = [o[:nranks * m] for o in outs]
+    if wc is not None:
+        wc = [c[:m] for c in wc]
+        ws = [s[:nblocks(m, block)] for s in ws]
+    return outs, wc, ws
+
+
+def all_to_all(inputs, block=BLOCK):
+    """LP AlltoAll: input r is N chunks of c = size/N elements. Returns
+    (outputs, wire_codes (N*c bytes each), wire_scales (N*ceil(c/128)))."""
+    inputs = [np.ascontiguousarray(x) for x in inputs]
+    nranks = len(inputs)
+    if inputs[0].size % nranks:
+        raise ValueError("all_to_all input length must be a multiple of N")
+    c = inputs[0].size // nranks
+    outs = [np.zeros(max(nranks * c, 1), dtype=inputs[0].dtype) for _ in range(nranks)]
+    if block:
+        nbc = nblocks(c, block)
+        wc = [np.zeros(max(nranks * c, 1), dtype=np.uint8) for _ in range(nranks)]
+        ws = [np.zeros(max(nranks * nbc, 1), dtype=np.float32) for _ in range(nranks)]
+    else:
+        wc = ws = None
+    null = (ctypes.c_void_p * nranks)()
+    _check(lib().orc_all_to_all(_ptrs(inputs), _ptrs(outs), nranks, c,
+                                _dtype_code(inputs[0]), block,
+                                _ptrs(wc) if wc else null,
+                                _ptrs(ws) if ws else null), "all_to_all")
+    outs = [o[:nranks * c] for o in outs]
+    if wc is not None:
+        wc = [x[:nranks * c] for x in wc]
+        ws = [x[:nranks * nblocks(c, block)] for x in ws]
+    return outs, wc, ws
 
 
 def shard_len(n, nranks, block=BLOCK):

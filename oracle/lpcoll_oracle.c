@@ -21,8 +21,10 @@
  *           bullets "Algoritmo DDA Flat" and "Algoritmo DDA Tree";
  *        "Funcionalidade Principal 2: Coletivos de Baixa Precisao",
  *           the paragraph on FP8 compression of >= 16 MB messages and the
- *           feature table rows "Tipos de Dados" (FP32, BF16 via FP8) and
- *           "Precisao do Calculo" (FP32 kept for the arithmetic);
+ *           feature table rows "Tipos de Dados" (FP32, BF16 via FP8),
+ *           "Precisao do Calculo" (FP32 kept for the arithmetic) and
+ *           "Operacoes Suportadas" (AllReduce, AllGather, AlltoAll,
+ *           ReduceScatter);
  *        "Guia Pratico e Perspectivas", the torch.full / allreduce(SUM)
  *           example.
  *
@@ -393,5 +395,140 @@ int orc_tree(const void *const *in, void *const *out, int nranks, size_t n,
             store_elem(out[dst], dtype, i,
                        dequant_elem(shard_codes, shard_scales, block, i));
     free(reduced);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The other low-precision collectives of [CJ] "Funcionalidade Principal 2", */
+/* feature table row "Operacoes Suportadas": ReduceScatter, AllGather,       */
+/* AlltoAll. Each rank publishes the FP8 payload of what it sends; the       */
+/* receivers dequantize it.                                                  */
+/* ------------------------------------------------------------------------ */
+
+static size_t elem_size(int dtype) { return dtype == ORC_F32 ? 4 : 2; }
+
+static const void *elem_ptr(const void *buf, int dtype, size_t i)
+{
+    return (const char *)buf + i * elem_size(dtype);
+}
+
+/* ReduceScatter: rank r ends with shard r (as defined by orc_shard_len) of
+ * the sum over ranks. block == 128: every rank first publishes its payload
+ * (wire_codes[r], wire_scales[r]); owner r then sums shard r of the N
+ * dequantized payloads in rank order. block == 0: the inputs are summed
+ * exactly. out[r] receives the min(L, n - rL) elements of shard r. */
+int orc_reduce_scatter(const void *const *in, void *const *out, int nranks,
+                       size_t n, int dtype, int block, uint8_t *const *wire_codes,
+                       float *const *wire_scales)
+{
+    size_t per, lo, hi, i;
+    int r, owner, st;
+    if (nranks < 1 || check_dtype(dtype))
+        return ORC_ERR_ARG;
+    if (block != 0 && check_block(block))
+        return ORC_ERR_UNSUPPORTED;
+    if (n == 0)
+        return ORC_OK;
+    per = orc_shard_len(n, nranks, block);
+    if (block) {
+        for (r = 0; r < nranks; r++) {
+            st = orc_quantize(in[r], dtype, n, block, wire_codes[r], wire_scales[r]);
+            if (st)
+                return st;
+        }
+    }
+    for (owner = 0; owner < nranks; owner++) {
+        lo = (size_t)owner * per;
+        hi = lo + per < n ? lo + per : n;
+        for (i = lo; i < hi; i++) {
+            float sum;
+            if (block) {
+                sum = dequant_elem(wire_codes[0], wire_scales[0], block, i);
+                for (r = 1; r < nranks; r++)
+                    sum = sum + dequant_elem(wire_codes[r], wire_scales[r], block, i);
+            } else {
+                sum = load_elem(in[0], dtype, i);
+                for (r = 1; r < nranks; r++)
+                    sum = sum + load_elem(in[r], dtype, i);
+            }
+            store_elem(out[owner], dtype, i - lo, sum);
+        }
+    }
+    return ORC_OK;
+}
+
+/* AllGather: rank r contributes m elements; every rank receives all N
+ * contributions in rank order, out[d][r*m + i] = contribution r, element i.
+ * block == 128: each rank publishes its contribution's payload (blocks
+ * counted from the start of the contribution) and the receivers dequantize
+ * it, so rank r's own copy is the dequantized value too. block == 0: exact
+ * copies. */
+int orc_all_gather(const void *const *in, void *const *out, int nranks, size_t m,
+                   int dtype, int block, uint8_t *const *wire_codes,
+                   float *const *wire_scales)
+{
+    size_t i;
+    int r, dst, st;
+    if (nranks < 1 || check_dtype(dtype))
+        return ORC_ERR_ARG;
+    if (block != 0 && check_block(block))
+        return ORC_ERR_UNSUPPORTED;
+    if (m == 0)
+        return ORC_OK;
+    if (block) {
+        for (r = 0; r < nranks; r++) {
+            st = orc_quantize(in[r], dtype, m, block, wire_codes[r], wire_scales[r]);
+            if (st)
+                return st;
+        }
+    }
+    for (dst = 0; dst < nranks; dst++)
+        for (r = 0; r < nranks; r++)
+            for (i = 0; i < m; i++) {
+                float v = block ? dequant_elem(wire_codes[r], wire_scales[r], block, i)
+                                : load_elem(in[r], dtype, i);
+                store_elem(out[dst], dtype, (size_t)r * m + i, v);
+            }
+    return ORC_OK;
+}
+
+/* AlltoAll: rank r's input is N chunks of c elements, chunk j addressed to
+ * rank j; rank j's output holds the chunks it received in sender order,
+ * out[j][r*c + i] = chunk j of rank r, element i. block == 128: rank r
+ * publishes one payload per destination chunk (blocks counted from the start
+ * of each chunk; chunk j's codes at wire_codes[r] + j*c, its scales at
+ * wire_scales[r] + j*ceil(c/128)) and the receivers dequantize them.
+ * block == 0: exact copies. */
+int orc_all_to_all(const void *const *in, void *const *out, int nranks, size_t c,
+                   int dtype, int block, uint8_t *const *wire_codes,
+                   float *const *wire_scales)
+{
+    size_t i, nbc;
+    int r, j, st;
+    if (nranks < 1 || check_dtype(dtype))
+        return ORC_ERR_ARG;
+    if (block != 0 && check_block(block))
+        return ORC_ERR_UNSUPPORTED;
+    if (c == 0)
+        return ORC_OK;
+    nbc = block ? (c + (size_t)block - 1) / (size_t)block : 0;
+    if (block) {
+        for (r = 0; r < nranks; r++)
+            for (j = 0; j < nranks; j++) {
+                st = orc_quantize(elem_ptr(in[r], dtype, (size_t)j * c), dtype, c, block,
+                                  wire_codes[r] + (size_t)j * c,
+                                  wire_scales[r] + (size_t)j * nbc);
+                if (st)
+                    return st;
+            }
+    }
+    for (j = 0; j < nranks; j++)
+        for (r = 0; r < nranks; r++)
+            for (i = 0; i < c; i++) {
+                float v = block ? dequant_elem(wire_codes[r] + (size_t)j * c,
+                                               wire_scales[r] + (size_t)j * nbc, block, i)
+                                : load_elem(in[r], dtype, (size_t)j * c + i);
+                store_elem(out[j], dtype, (size_t)r * c + i, v);
+            }
     return ORC_OK;
 }

@@ -508,4 +508,97 @@ def pin_shard_len(oracle):
         assert oracle.shard_len(n, N, block) == want, (n, N, block)
 
 
+# -- ReduceScatter, AllGather, AlltoAll -------------------------------------
+
+def _representable(n, seed, dt, j=0):
+    """n elements that are E4M3 values times 2^j, with 448 * 2^j in every
+    128-block (so every block's scale is exactly 2^j and the payload round
+    trip is exact)."""
+    g = np.random.default_rng(seed)
+    table = torch_e4m3_table()
+    valid = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    x = (table[g.choice(valid, size=n)] * np.float32(2.0 ** j)).astype(np.float32)
+    x[::128] = np.float32(448.0 * 2.0 ** j)
+    return torch_bf16_bits(x) if dt == BF16 else x
+
+
+def pin_reduce_scatter(oracle):
+    for dt in (F32, BF16):
+        for N, n in ((1, 300), (3, 1000), (8, 129), (5, 128 * 40 + 1)):
+            ins = W.random_inputs(N, n, dt, 300 + N + n, scale_spread=3.0)
+            outs, wc, ws = oracle.reduce_scatter(ins)
+            per = oracle.shard_len(n, N)
+            T, bound = _bounds(ins, ws, ins[0].dtype)
+            for r in range(N):
+                lo, hi = r * per, min(n, (r + 1) * per)
+                assert outs[r].size == max(0, hi - lo)
+                if hi > lo:
+                    err = np.abs(widen(outs[r]).astype(np.float64) - T[lo:hi])
+                    assert np.all(err <= bound[lo:hi]), (N, n, r)
+            flat = oracle.flat(ins)[0][0]
+            for r in range(N):
+                lo = r * per
+                assert same_bits(outs[r], flat[lo:lo + outs[r].size])
+            if N == 1:
+                c, s = oracle.quantize(ins[0])
+                assert same_bits(outs[0], oracle.dequantize(c, s, dtype=ins[0].dtype))
+    for N, rows, cols, want in read_torch_full_cases():
+        ins = W.torch_full_example(N, (rows, cols))
+        outs = oracle.reduce_scatter(ins, block=0)[0]
+        assert sum(o.size for o in outs) == rows * cols
+        assert all(np.all(o == np.float32(want)) for o in outs)
+
+
+def pin_all_gather(oracle):
+    for dt in (F32, BF16):
+        for N, m in ((1, 200), (3, 128), (4, 300), (8, 77)):
+            # exactly representable contributions come back unchanged
+            ins = [_representable(m, 400 + r, dt, j=3 * r - 4) for r in range(N)]
+            outs, wc, ws = oracle.all_gather(ins)
+            cat = np.concatenate(ins)
+            for o in outs:
+                assert same_bits(o, cat), (N, m)
+            assert all(same_bits(o, cat) for o in oracle.all_gather(ins, block=0)[0])
+            # general contributions: each segment within the quantization bound
+            ins = W.random_inputs(N, m, dt, 500 + N, scale_spread=3.0)
+            outs, wc, ws = oracle.all_gather(ins)
+            for r in range(N):
+                seg = outs[0][r * m:(r + 1) * m]
+                x = widen(ins[r]).astype(np.float64)
+                T, bound = _bounds([ins[r]], [ws[r]], ins[0].dtype)
+                assert np.all(np.abs(widen(seg).astype(np.float64) - x) <= bound)
+            for o in outs[1:]:
+                assert same_bits(o, outs[0])
+
+
+def pin_all_to_all(oracle):
+    for dt in (F32, BF16):
+        for N, c in ((1, 256), (2, 200), (4, 128), (3, 130)):
+            ins = [np.concatenate([_representable(c, 600 + 10 * r + j, dt, j=r - j)
+                                   for j in range(N)]) for r in range(N)]
+            for block in (128, 0):
+                outs = oracle.all_to_all(ins, block=block)[0]
+                for j in range(N):
+                    for r in range(N):
+                        assert same_bits(outs[j][r * c:(r + 1) * c],
+                                         ins[r][j * c:(j + 1) * c]), (N, c, j, r, block)
+        # blocks restart at every chunk: chunk j's first scale is the largest
+        # magnitude of its own first (up to) 128 elements over 448
+        N, c = 3, 200
+        ins = W.random_inputs(N, N * c, dt, 700, scale_spread=3.0)
+        outs, wc, ws = oracle.all_to_all(ins)
+        nbc = (c + 127) // 128
+        for r in range(N):
+            x = widen(ins[r])
+            for j in range(N):
+                first = x[j * c:j * c + 128]
+                tail = x[j * c + 128:(j + 1) * c]
+                assert ws[r][j * nbc] == np.float32(np.max(np.abs(first))) / np.float32(448.0)
+                assert ws[r][j * nbc + 1] == np.float32(np.max(np.abs(tail))) / np.float32(448.0)
+                T, bound = _bounds([ins[r][j * c:(j + 1) * c]], [ws[r][j * nbc:(j + 1) * nbc]],
+                                   ins[0].dtype)
+                got = widen(outs[j][r * c:(r + 1) * c]).astype(np.float64)
+                assert np.all(np.abs(got - T) <= bound)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

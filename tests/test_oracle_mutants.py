@@ -45,6 +45,18 @@ MUTANTS = [
      "        per = (per + (size_t)block - 1) / (size_t)block * (size_t)block;",
      "        per = per;"),
     ("subnormal_sign_lost", "        return sign | (uint8_t)m;", "        return (uint8_t)m;"),
+    ("rs_wrong_offset", "            store_elem(out[owner], dtype, i - lo, sum);",
+     "            store_elem(out[owner], dtype, i - lo + (owner > 0), sum);"),
+    ("ag_own_contribution",
+     "                float v = block ? dequant_elem(wire_codes[r], wire_scales[r], block, i)\n                                : load_elem(in[r], dtype, i);",
+     "                float v = block ? dequant_elem(wire_codes[dst], wire_scales[dst], block, i)\n                                : load_elem(in[dst], dtype, i);"),
+    ("a2a_transposed",
+     "                store_elem(out[j], dtype, (size_t)r * c + i, v);",
+     "                store_elem(out[r], dtype, (size_t)j * c + i, v);"),
+    ("a2a_global_blocks",
+     "                st = orc_quantize(elem_ptr(in[r], dtype, (size_t)j * c), dtype, c, block,\n                                  wire_codes[r] + (size_t)j * c,\n                                  wire_scales[r] + (size_t)j * nbc);",
+     "                st = j ? 0 : orc_quantize(in[r], dtype, c * (size_t)nranks, block,\n                                          wire_codes[r], wire_scales[r]);"),
+], dtype, c * (size_t)nranks, block, wire_codes[r], wire_scales[r]); break; }"),
 ]
 
 
