@@ -56,7 +56,6 @@ MUTANTS = [
     ("a2a_global_blocks",
      "                st = orc_quantize(elem_ptr(in[r], dtype, (size_t)j * c), dtype, c, block,\n                                  wire_codes[r] + (size_t)j * c,\n                                  wire_scales[r] + (size_t)j * nbc);",
      "                st = j ? 0 : orc_quantize(in[r], dtype, c * (size_t)nranks, block,\n                                          wire_codes[r], wire_scales[r]);"),
-], dtype, c * (size_t)nranks, block, wire_codes[r], wire_scales[r]); break; }"),
 ]
 
 
