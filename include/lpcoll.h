@@ -133,6 +133,59 @@ int dda_tree_sim(const void *const *in, void *const *out, int nranks,
                  uint8_t *const *wire_codes, float *const *wire_scales,
                  uint8_t *shard_codes, float *shard_scales, void *stream);
 
+/* ReduceScatter over nranks emulated ranks: rank r receives shard r of the
+ * sum of all ranks' messages. Pages: "Funcionalidade Principal 2", feature
+ * table row "Operacoes Suportadas" (ReduceScatter).
+ * Shard r is elements [r L, min((r+1) L, n)); L = ceil(n/nranks), rounded
+ * up to a multiple of 128 when block = 128.
+ *   in[r]       rank r's message, n elements of dtype (device)
+ *   out[r]      shard r of the result, min(L, n - r L) elements (device);
+ *               may be NULL when that count is <= 0
+ *   block = 128: each rank's message is quantized into wire_codes[r] (n
+ *               bytes) / wire_scales[r] (ceil(n/128) floats), and shard r is
+ *               the FP32 sum of the dequantized payloads (rank order, cast
+ *               to dtype): bit-equal to that shard of dda_flat_sim's output.
+ *   block = 0:  exact FP32 sum of the inputs; wires ignored (may be NULL). */
+int reduce_scatter_sim(const void *const *in, void *const *out, int nranks,
+                       size_t n, lpcoll_dtype dtype, int block,
+                       uint8_t *const *wire_codes, float *const *wire_scales,
+                       void *stream);
+
+/* AllGather: every rank receives all ranks' contributions in rank order.
+ * Pages: "Operacoes Suportadas" (AllGather).
+ *   in[r]       rank r's contribution, m elements of dtype (device)
+ *   out[r]      nranks * m elements (device): out[r][q m + i] = contribution
+ *               q, element i, for every r
+ *   block = 128: each contribution is quantized on its own 128-element
+ *               blocks into wire_codes[r] (m bytes) / wire_scales[r]
+ *               (ceil(m/128) floats); every output, the sender's own
+ *               included, holds the dequantized values.
+ *   block = 0:  exact copies; wires ignored (may be NULL).
+ * Any m works; when m * element size is not a multiple of 16 bytes the
+ * outputs are written element by element (slower).                        */
+int all_gather_sim(const void *const *in, void *const *out, int nranks,
+                   size_t m, lpcoll_dtype dtype, int block,
+                   uint8_t *const *wire_codes, float *const *wire_scales,
+                   void *stream);
+
+/* AlltoAll: rank r's message is nranks chunks of c elements, chunk j
+ * addressed to rank j. Pages: "Operacoes Suportadas" (AlltoAll).
+ *   in[r]       nranks * c elements of dtype (device)
+ *   out[j]      nranks * c elements (device): out[j][r c + i] = chunk j of
+ *               rank r, element i
+ *   block = 128: every chunk is quantized on its own 128-element blocks
+ *               (counted from the chunk's start): chunk j of rank r has its
+ *               codes at wire_codes[r] + j c (nranks * c bytes in all) and
+ *               its scales at wire_scales[r] + j ceil(c/128) (nranks *
+ *               ceil(c/128) floats); receivers get the dequantized values.
+ *   block = 0:  exact copies; wires ignored (may be NULL).
+ * Any c works; when c * element size is not a multiple of 16 bytes the data
+ * moves element by element (slower).                                      */
+int all_to_all_sim(const void *const *in, void *const *out, int nranks,
+                   size_t c, lpcoll_dtype dtype, int block,
+                   uint8_t *const *wire_codes, float *const *wire_scales,
+                   void *stream);
+
 /* dda_flat_sim with block = 128 for callers that cannot allocate device
  * memory. The pages have no counterpart: this exists for users of the
  * library, not for the method. Some callers cannot provide the wire buffers

@@ -6,11 +6,14 @@ ABI in include/lpcoll.h); this package is its binding (``_binding``), an
 in-place allreduce facade (``allreduce``), the build step (``build``) and the
 seeded workload generators (``workloads``).
 """
-from ._binding import (BF16, BLOCK, F32, MAX_RANKS, LpcollError, dda_flat_sim,
+from ._binding import (BF16, BLOCK, F32, MAX_RANKS, LpcollError, all_gather_sim,
+                       all_to_all_sim, dda_flat_sim, dda_flat_sim_noalloc,
                        dda_tree_sim, lib, lp_dequantize, lp_quantize, lp_reduce,
-                       nblocks, status_string)
+                       nblocks, reduce_scatter_sim, shard_len, status_string)
 from .allreduce import Workspace, allreduce_sim, choose
 
 __all__ = ["BF16", "BLOCK", "F32", "MAX_RANKS", "LpcollError", "Workspace",
-           "allreduce_sim", "choose", "dda_flat_sim", "dda_tree_sim", "lib",
-           "lp_dequantize", "lp_quantize", "lp_reduce", "nblocks", "status_string"]
+           "all_gather_sim", "all_to_all_sim", "allreduce_sim", "choose",
+           "dda_flat_sim", "dda_flat_sim_noalloc", "dda_tree_sim", "lib",
+           "lp_dequantize", "lp_quantize", "lp_reduce", "nblocks",
+           "reduce_scatter_sim", "shard_len", "status_string"]

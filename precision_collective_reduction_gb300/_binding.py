@@ -47,8 +47,13 @@ def lib():
         L.lp_reduce.argtypes = [pp, pp, ci, sz, ci, vp, ci, vp]
         L.dda_flat_sim.argtypes = [pp, pp, ci, sz, ci, ci, pp, pp, vp]
         L.dda_tree_sim.argtypes = [pp, pp, ci, sz, ci, ci, pp, pp, vp, vp, vp]
+        for f in ("reduce_scatter_sim", "all_gather_sim", "all_to_all_sim"):
+            getattr(L, f).argtypes = [pp, pp, ci, sz, ci, ci, pp, pp, vp]
+        L.dda_flat_sim_noalloc.argtypes = [pp, pp, ci, sz, ci, vp]
         for f in ("lp_quantize", "lp_dequantize", "lp_reduce", "dda_flat_sim",
-                  "dda_tree_sim", "lpcoll_last_cuda_error", "lpcoll_version"):
+                  "dda_tree_sim", "reduce_scatter_sim", "all_gather_sim",
+                  "all_to_all_sim", "dda_flat_sim_noalloc",
+                  "lpcoll_last_cuda_error", "lpcoll_version"):
             getattr(L, f).restype = ci
         L.lpcoll_status_string.argtypes = [ci]
         L.lpcoll_status_string.restype = ctypes.c_char_p
@@ -103,6 +108,19 @@ def raw_dda_tree_sim(in_ptrs, out_ptrs, nranks, n, dtype, block, wc_ptrs, ws_ptr
     _check(lib().dda_tree_sim(ptr_array(in_ptrs), ptr_array(out_ptrs), nranks, n,
                               dtype, block, ptr_array(wc_ptrs), ptr_array(ws_ptrs),
                               sc_ptr, ss_ptr, stream), "dda_tree_sim")
+
+
+def raw_collective(name, in_ptrs, out_ptrs, nranks, count, dtype, block, wc_ptrs,
+                   ws_ptrs, stream):
+    """reduce_scatter_sim / all_gather_sim / all_to_all_sim by name."""
+    _check(getattr(lib(), name)(ptr_array(in_ptrs), ptr_array(out_ptrs), nranks, count,
+                                dtype, block, ptr_array(wc_ptrs), ptr_array(ws_ptrs),
+                                stream), name)
+
+
+def raw_dda_flat_sim_noalloc(in_ptrs, out_ptrs, nranks, n, dtype, stream):
+    _check(lib().dda_flat_sim_noalloc(ptr_array(in_ptrs), ptr_array(out_ptrs), nranks,
+                                      n, dtype, stream), "dda_flat_sim_noalloc")
 
 
 # -- torch-tensor calls -----------------------------------------------------
@@ -228,4 +246,91 @@ def dda_tree_sim(ins, outs, block=BLOCK, wire_codes=None, wire_scales=None,
         sc = _need(shard_codes, "shard_codes", torch.uint8, n)
         ss = _need(shard_scales, "shard_scales", torch.float32, nblocks(n, block))
     raw_dda_tree_sim(ip, op, len(ip), n, dt, block, wc, ws, sc, ss, _stream(stream))
+    return outs
+
+
+def shard_len(n, nranks, block=BLOCK):
+    """Elements per reduce-scatter shard (the last shard may be shorter)."""
+    per = -(-n // nranks)
+    return -(-per // block) * block if block else per
+
+
+def _wire_args(ins, wire_codes, wire_scales, block, ncodes, nscales):
+    torch = _torch()
+    if not block:
+        return [], []
+    if wire_codes is None or wire_scales is None:
+        raise ValueError("low precision (block=128) needs wire_codes and wire_scales")
+    if len(wire_codes) != len(ins) or len(wire_scales) != len(ins):
+        raise ValueError("one wire payload per rank")
+    wc = [_need(t, "wire_codes[%d]" % r, torch.uint8, ncodes)
+          for r, t in enumerate(wire_codes)]
+    ws = [_need(t, "wire_scales[%d]" % r, torch.float32, nscales)
+          for r, t in enumerate(wire_scales)]
+    return wc, ws
+
+
+def _inputs(ins, count):
+    dt = ins[0].dtype
+    ip = [_need(t, "in[%d]" % r, dt, None) for r, t in enumerate(ins)]
+    if any(t.numel() != count for t in ins):
+        raise ValueError("every rank's input must have %d elements" % count)
+    return ip, dt
+
+
+def reduce_scatter_sim(ins, outs, block=BLOCK, wire_codes=None, wire_scales=None,
+                       stream=None):
+    """ReduceScatter: outs[r] (shard_len elements, the last rank's fewer; may
+    be None for an empty shard) receives shard r of the sum of ``ins``."""
+    N = len(ins)
+    n = ins[0].numel()
+    ip, dt = _inputs(ins, n)
+    per = shard_len(n, N, block) if n else 0
+    op = []
+    for r, t in enumerate(outs):
+        k = max(0, min(per, n - r * per))
+        op.append(0 if (t is None and k == 0) else _need(t, "out[%d]" % r, dt, k))
+    wc, ws = _wire_args(ins, wire_codes, wire_scales, block, n, nblocks(n))
+    raw_collective("reduce_scatter_sim", ip, op, N, n, dtype_code(ins[0]), block, wc, ws,
+                   _stream(stream))
+    return outs
+
+
+def all_gather_sim(ins, outs, block=BLOCK, wire_codes=None, wire_scales=None,
+                   stream=None):
+    """AllGather: every outs[r] (N*m elements) receives all N contributions."""
+    N = len(ins)
+    m = ins[0].numel()
+    ip, dt = _inputs(ins, m)
+    op = [_need(t, "out[%d]" % r, dt, N * m) for r, t in enumerate(outs)]
+    wc, ws = _wire_args(ins, wire_codes, wire_scales, block, m, nblocks(m))
+    raw_collective("all_gather_sim", ip, op, N, m, dtype_code(ins[0]), block, wc, ws,
+                   _stream(stream))
+    return outs
+
+
+def all_to_all_sim(ins, outs, block=BLOCK, wire_codes=None, wire_scales=None,
+                   stream=None):
+    """AlltoAll: ins[r] is N chunks of c elements; outs[j][r*c:(r+1)*c] receives
+    chunk j of rank r."""
+    N = len(ins)
+    total = ins[0].numel()
+    if total % N:
+        raise ValueError("all_to_all input length must be a multiple of N")
+    c = total // N
+    ip, dt = _inputs(ins, total)
+    op = [_need(t, "out[%d]" % r, dt, total) for r, t in enumerate(outs)]
+    wc, ws = _wire_args(ins, wire_codes, wire_scales, block, total, N * nblocks(c))
+    raw_collective("all_to_all_sim", ip, op, N, c, dtype_code(ins[0]), block, wc, ws,
+                   _stream(stream))
+    return outs
+
+
+def dda_flat_sim_noalloc(ins, outs, stream=None):
+    """dda_flat_sim with block=128 whose wires live in the library's own
+    fixed device array (for callers that cannot allocate device memory)."""
+    n = ins[0].numel()
+    ip, dt = _inputs(ins, n)
+    op = [_need(t, "out[%d]" % r, dt, n) for r, t in enumerate(outs)]
+    raw_dda_flat_sim_noalloc(ip, op, len(ip), n, dtype_code(ins[0]), _stream(stream))
     return outs

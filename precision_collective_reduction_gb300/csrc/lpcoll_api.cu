@@ -20,6 +20,10 @@ cudaError_t launch_dequantize(const uint8_t *codes, const float *scales, size_t 
                               void *out, int dtype, cudaStream_t stream);
 cudaError_t launch_reduce(const ReduceParams &p, int nranks, size_t n, void *out,
                           int dtype, cudaStream_t stream);
+cudaError_t launch_all_gather(const DdaParams &p, int nranks, size_t m, int dtype,
+                              bool lp, cudaStream_t st);
+cudaError_t launch_all_to_all(const DdaParams &p, int nranks, size_t c, int dtype,
+                              bool lp, cudaStream_t st);
 
 namespace {
 
@@ -151,6 +155,48 @@ int dda_common(const void *const *in, void *const *out, int nranks, size_t n,
                                       : launch_dda_bf16(p, nranks, n, mode, s));
 }
 
+// Checks shared by the collectives other than the allreduce; fills the
+// per-rank pointers of p. out[r] may be NULL where out_empty(r) is true.
+template <class Empty>
+int collective_args(const void *const *in, void *const *out, int nranks, int dtype,
+                    int block, uint8_t *const *wire_codes, float *const *wire_scales,
+                    Empty out_empty, DdaParams &p)
+{
+    int st = first_error({
+        check_rank_array(in, nranks),
+        block ? check_rank_array(wire_codes, nranks) : LPCOLL_OK,
+        block ? check_rank_array(wire_scales, nranks) : LPCOLL_OK,
+    });
+    if (st != LPCOLL_OK)
+        return st;
+    if (out == nullptr)
+        return LPCOLL_ERR_ARG;
+    for (int r = 0; r < nranks; ++r)
+        if (out[r] == nullptr && !out_empty(r))
+            return LPCOLL_ERR_RANK;
+    for (int r = 0; r < nranks; ++r)
+        if (out[r] != nullptr && misaligned(out[r]))
+            return LPCOLL_ERR_ALIGN;
+    for (int r = 0; r < nranks; ++r) {
+        p.in[r] = in[r];
+        p.out[r] = out[r];
+        if (block) {
+            p.codes[r] = wire_codes[r];
+            p.scales[r] = wire_scales[r];
+        }
+    }
+    return LPCOLL_OK;
+}
+
+int check_common(int dtype, int nranks, int block)
+{
+    if (bad_dtype(dtype) || nranks < 1 || nranks > LPCOLL_MAX_RANKS)
+        return LPCOLL_ERR_ARG;
+    if (block != 0 && block != LPCOLL_BLOCK)
+        return LPCOLL_ERR_UNSUPPORTED;
+    return LPCOLL_OK;
+}
+
 }  // namespace
 
 int wave_ctas(const void *kernel, size_t units)
@@ -236,6 +282,59 @@ int dda_tree_sim(const void *const *in, void *const *out, int nranks, size_t n,
 {
     return dda_common(in, out, nranks, n, dtype, block, wire_codes, wire_scales,
                       shard_codes, shard_scales, true, stream);
+}
+
+int reduce_scatter_sim(const void *const *in, void *const *out, int nranks, size_t n,
+                       lpcoll_dtype dtype, int block, uint8_t *const *wire_codes,
+                       float *const *wire_scales, void *stream)
+{
+    int st = check_common(dtype, nranks, block);
+    if (st != LPCOLL_OK || n == 0)
+        return st;
+    size_t per = (n + static_cast<size_t>(nranks) - 1) / static_cast<size_t>(nranks);
+    if (block)
+        per = (per + LPCOLL_BLOCK - 1) / LPCOLL_BLOCK * LPCOLL_BLOCK;
+    DdaParams p = {};
+    st = collective_args(in, out, nranks, dtype, block, wire_codes, wire_scales,
+                         [&](int r) { return static_cast<size_t>(r) * per >= n; }, p);
+    if (st != LPCOLL_OK)
+        return st;
+    p.shard_len = per;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish(dtype == LPCOLL_F32 ? launch_scatter_f32(p, nranks, n, block != 0, s)
+                                      : launch_scatter_bf16(p, nranks, n, block != 0, s));
+}
+
+int all_gather_sim(const void *const *in, void *const *out, int nranks, size_t m,
+                   lpcoll_dtype dtype, int block, uint8_t *const *wire_codes,
+                   float *const *wire_scales, void *stream)
+{
+    int st = check_common(dtype, nranks, block);
+    if (st != LPCOLL_OK || m == 0)
+        return st;
+    DdaParams p = {};
+    st = collective_args(in, out, nranks, dtype, block, wire_codes, wire_scales,
+                         [](int) { return false; }, p);
+    if (st != LPCOLL_OK)
+        return st;
+    return finish(launch_all_gather(p, nranks, m, dtype, block != 0,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+int all_to_all_sim(const void *const *in, void *const *out, int nranks, size_t c,
+                   lpcoll_dtype dtype, int block, uint8_t *const *wire_codes,
+                   float *const *wire_scales, void *stream)
+{
+    int st = check_common(dtype, nranks, block);
+    if (st != LPCOLL_OK || c == 0)
+        return st;
+    DdaParams p = {};
+    st = collective_args(in, out, nranks, dtype, block, wire_codes, wire_scales,
+                         [](int) { return false; }, p);
+    if (st != LPCOLL_OK)
+        return st;
+    return finish(launch_all_to_all(p, nranks, c, dtype, block != 0,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 const char *lpcoll_status_string(int status)

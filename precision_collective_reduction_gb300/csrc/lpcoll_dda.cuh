@@ -12,7 +12,8 @@
 //   4. tree only: requantizes the reduced block into the shard payload
 //      (reduce-scatter: the block's owner is the rank whose shard holds it)
 //      and replaces the sum by its dequantized value (all-gather);
-//   5. writes the result to all N outputs.
+//   5. writes the result to all N outputs, or, for a reduce-scatter, only to
+//      the output of the rank whose shard holds the element.
 // Every element is read before any output of its unit is written, so an
 // output may alias its input.
 //
@@ -25,12 +26,44 @@
 
 namespace lpc {
 
+// Reduce-scatter output: element e belongs to shard e / L and lands at
+// e - owner * L in the owner's output. A lane's kVec elements go out as one
+// 16-byte store when they lie in one shard at an aligned offset (always so
+// when L is a whole number of 128-element blocks), else one by one.
+template <int DT>
+__device__ __forceinline__ void scatter_store(const DdaParams &p, size_t e0, int cnt,
+                                              uint4 v)
+{
+    constexpr int V = Fmt<DT>::kVec;
+    constexpr int ES = 16 / V;
+    const size_t L = p.shard_len;
+    const size_t owner = e0 / L;
+    const size_t off = e0 - owner * L;
+    if (off + static_cast<size_t>(cnt) <= L && ((off * ES) & 15) == 0) {
+        store_vec<DT>(p.out[owner], off, cnt, v);
+        return;
+    }
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int j = 0; j < cnt; ++j) {
+        const size_t e = e0 + j;
+        const size_t o = e / L;
+        if (DT == LPCOLL_F32) {
+            static_cast<uint32_t *>(p.out[o])[e - o * L] = w[j];
+        } else {
+            static_cast<uint16_t *>(p.out[o])[e - o * L] =
+                static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+        }
+    }
+}
+
 template <int N, int DT, int MODE, bool FULL>
 __device__ __forceinline__ void dda_unit(const DdaParams &p, size_t n, size_t unit,
                                          int lane)
 {
     using F = Fmt<DT>;
     constexpr int V = F::kVec;
+    constexpr bool kExactSum = (MODE == kExact || MODE == kScatterExact);
+    constexpr bool kScatter = (MODE == kScatterExact || MODE == kScatterLp);
     const size_t e0 = (unit * 32 + lane) * V;
     const int cnt = FULL ? V : lane_count<DT>(n, e0);
     const bool leader = (lane % F::kGroup) == 0;
@@ -46,7 +79,7 @@ __device__ __forceinline__ void dda_unit(const DdaParams &p, size_t n, size_t un
     for (int r = 0; r < N; ++r) {
         float x[V];
         widen<DT>(raw[r], x);
-        if constexpr (MODE == kExact) {
+        if constexpr (kExactSum) {
 #pragma unroll
             for (int j = 0; j < V; ++j)
                 acc[j] = (r == 0) ? x[j] : __fadd_rn(acc[j], x[j]);
@@ -79,9 +112,13 @@ __device__ __forceinline__ void dda_unit(const DdaParams &p, size_t n, size_t un
 
     if (FULL || cnt > 0) {
         const uint4 o = narrow<DT>(acc);
+        if constexpr (kScatter) {
+            scatter_store<DT>(p, e0, cnt, o);
+        } else {
 #pragma unroll
-        for (int r = 0; r < N; ++r)
-            store_vec<DT>(p.out[r], e0, cnt, o);
+            for (int r = 0; r < N; ++r)
+                store_vec<DT>(p.out[r], e0, cnt, o);
+        }
     }
 }
 
@@ -151,10 +188,23 @@ cudaError_t launch_dda(const DdaParams &p, int nranks, size_t n, int mode,
     }
 }
 
-// Defined in lpcoll_dda_f32.cu / lpcoll_dda_bf16.cu.
+template <int DT>
+cudaError_t launch_scatter(const DdaParams &p, int nranks, size_t n, bool lp,
+                           cudaStream_t stream)
+{
+    return lp ? launch_dda_mode<DT, kScatterLp>(p, nranks, n, stream)
+              : launch_dda_mode<DT, kScatterExact>(p, nranks, n, stream);
+}
+
+// Defined in lpcoll_dda_f32.cu / lpcoll_dda_bf16.cu (allreduce) and
+// lpcoll_scatter_f32.cu / lpcoll_scatter_bf16.cu (reduce-scatter).
 cudaError_t launch_dda_f32(const DdaParams &p, int nranks, size_t n, int mode,
                            cudaStream_t stream);
 cudaError_t launch_dda_bf16(const DdaParams &p, int nranks, size_t n, int mode,
                             cudaStream_t stream);
+cudaError_t launch_scatter_f32(const DdaParams &p, int nranks, size_t n, bool lp,
+                               cudaStream_t stream);
+cudaError_t launch_scatter_bf16(const DdaParams &p, int nranks, size_t n, bool lp,
+                                cudaStream_t stream);
 
 }  // namespace lpc

@@ -31,7 +31,9 @@ constexpr int kWarpsPerCta = kThreads / 32;
 // enough 16-byte loads in flight and streamed HBM faster than 32 warps.
 constexpr int kCtasPerSm = 2;
 
-enum Mode { kExact = 0, kFlat = 1, kTree = 2 };
+// What a fused launch computes: the allreduce (exact, LP flat, LP tree) or a
+// reduce-scatter (exact or LP), whose result goes to the shard's owner only.
+enum Mode { kExact = 0, kFlat = 1, kTree = 2, kScatterExact = 3, kScatterLp = 4 };
 
 // Element format traits: elements per 16-byte vector and lanes per block.
 template <int DT> struct Fmt;
@@ -52,6 +54,7 @@ struct DdaParams {
     float *scales[LPCOLL_MAX_RANKS];
     uint8_t *shard_codes;
     float *shard_scales;
+    size_t shard_len;  // reduce-scatter: elements per shard (last one shorter)
 };
 
 // Per-rank payload pointers of lp_reduce.
@@ -77,6 +80,8 @@ __device__ __forceinline__ uint4 load_vec(const void *base, size_t e0, int cnt)
     const char *p = static_cast<const char *>(base) + e0 * ES;
     if (cnt == V)
         return *reinterpret_cast<const uint4 *>(p);
+    if (cnt < 0)  // a full lane at an address that is not 16-byte aligned
+        cnt = -cnt;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     uint32_t w[4] = {0u, 0u, 0u, 0u};
     if (DT == LPCOLL_F32) {
@@ -105,6 +110,8 @@ __device__ __forceinline__ void store_vec(void *base, size_t e0, int cnt, uint4 
         *reinterpret_cast<uint4 *>(p) = v;
         return;
     }
+    if (cnt < 0)  // a full lane at an address that is not 16-byte aligned
+        cnt = -cnt;
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     if (DT == LPCOLL_F32) {
         uint32_t *q = reinterpret_cast<uint32_t *>(p);
@@ -115,6 +122,22 @@ __device__ __forceinline__ void store_vec(void *base, size_t e0, int cnt, uint4 
         for (int j = 0; j < cnt; ++j)
             q[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
     }
+}
+
+// As load_vec / store_vec for element offsets that may not be 16-byte
+// aligned: vector access only when `aligned` (uniform per launch) holds.
+template <int DT>
+__device__ __forceinline__ uint4 load_any(const void *base, size_t e0, int cnt,
+                                          bool aligned)
+{
+    return load_vec<DT>(base, e0, aligned ? cnt : (cnt == Fmt<DT>::kVec ? -cnt : cnt));
+}
+
+template <int DT>
+__device__ __forceinline__ void store_any(void *base, size_t e0, int cnt, uint4 v,
+                                          bool aligned)
+{
+    store_vec<DT>(base, e0, aligned ? cnt : (cnt == Fmt<DT>::kVec ? -cnt : cnt), v);
 }
 
 // kVec codes of one lane, packed little-endian (element e0 in the low byte).
@@ -133,6 +156,8 @@ __device__ __forceinline__ void store_codes(uint8_t *base, size_t e0, int cnt,
         __stcs(reinterpret_cast<unsigned int *>(base + e0), c.w);
         return;
     }
+    if (cnt < 0)
+        cnt = -cnt;
     for (int j = 0; j < cnt; ++j)
         base[e0 + j] = static_cast<uint8_t>(c.w >> (8 * j));
 }
@@ -144,6 +169,8 @@ __device__ __forceinline__ void store_codes(uint8_t *base, size_t e0, int cnt,
         __stcs(reinterpret_cast<uint2 *>(base + e0), c.w);
         return;
     }
+    if (cnt < 0)
+        cnt = -cnt;
     for (int j = 0; j < cnt; ++j) {
         uint32_t word = j < 4 ? c.w.x : c.w.y;
         base[e0 + j] = static_cast<uint8_t>(word >> (8 * (j & 3)));

@@ -1,0 +1,10 @@
+// BF16 instantiations of the fused reduce-scatter kernels (N = 1..16).
+#include "lpcoll_dda.cuh"
+
+namespace lpc {
+cudaError_t launch_scatter_bf16(const DdaParams &p, int nranks, size_t n, bool lp,
+                                cudaStream_t stream)
+{
+    return launch_scatter<LPCOLL_BF16>(p, nranks, n, lp, stream);
+}
+}  // namespace lpc

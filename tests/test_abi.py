@@ -125,3 +125,35 @@ def test_library_is_built_for_sm103a():
     assert "arch=compute_103a,code=sm_103a" in " ".join(lib_build.NVCC_FLAGS)
     assert os.path.getsize(lib_build.LIB) > 0
     ctypes.CDLL(lib_build.LIB)
+
+
+@pytest.mark.parametrize("fn", ["reduce_scatter_sim", "all_gather_sim", "all_to_all_sim"])
+def test_collective_validation(L, fn):
+    f = getattr(L, fn)
+    two = arr(A, A)
+    assert f(two, two, 2, 10, 3, 128, two, two, None) == ARG        # dtype
+    assert f(two, two, 0, 10, 0, 128, two, two, None) == ARG        # N < 1
+    assert f(two, two, 17, 10, 0, 128, two, two, None) == ARG       # N > 16
+    assert f(two, two, 2, 10, 0, 256, two, two, None) == UNSUP      # block
+    assert f(None, None, 2, 0, 0, 128, None, None, None) == OK      # empty: no-op
+    assert f(None, two, 2, 10, 0, 0, None, None, None) == ARG
+    assert f(arr(A, None), two, 2, 10, 0, 0, None, None, None) == RANK
+    assert f(two, None, 2, 10, 0, 0, None, None, None) == ARG
+    assert f(two, two, 2, 10, 0, 128, None, two, None) == ARG       # LP needs wires
+    assert f(two, two, 2, 10, 1, 128, two, arr(None, A), None) == RANK
+    assert f(two, arr(A, A + 4), 2, 10, 0, 0, None, None, None) == ALIGN
+    assert f(two, two, 2, 10, 0, 128, arr(A + 2, A), two, None) == ALIGN
+    if fn == "reduce_scatter_sim":
+        # n = 10 over 8 ranks: shards of 2 elements, ranks 5..7 empty. Their
+        # outputs may be NULL: the call gets past the NULL checks and stops at
+        # the misaligned out[0] (nothing is launched), while a NULL output of
+        # a non-empty shard is refused.
+        eight = arr(*([A] * 8))
+        assert f(eight, arr(A + 4, A, A, A, A, None, None, None), 8, 10, 0, 0, None,
+                 None, None) == ALIGN
+        assert f(eight, arr(A + 4, None, A, A, A, A, A, A), 8, 10, 0, 0, None, None,
+                 None) == RANK
+        assert f(eight, arr(*([A] + [None] * 7)), 8, 10, 0, 128, None, None,
+                 None) == ARG                                       # wires first
+    else:
+        assert f(two, arr(A, None), 2, 10, 0, 0, None, None, None) == RANK
