@@ -366,6 +366,71 @@ def measure_small(torch, w, stream, iters, graph_replays=0):
     return out
 
 
+def collective_bytes(kind, N, count, elem, block):
+    """Algorithmic HBM bytes of one reduce-scatter (count = n per rank),
+    all-gather (count = m per contribution) or all-to-all (count = c per
+    chunk): inputs read once, wires written once, outputs written once."""
+    def wire(k):
+        return (k + 4 * ((k + 127) // 128)) if block else 0
+    if kind == "reduce_scatter":
+        return N * count * elem + N * wire(count) + count * elem
+    if kind == "all_gather":
+        return N * count * elem + N * wire(count) + N * N * count * elem
+    return N * N * count * elem + N * N * wire(count) + N * N * count * elem
+
+
+def measure_collectives(torch, stream, iters=20):
+    """ReduceScatter / AllGather / AlltoAll, LP, 8 ranks, 16 MiB BF16 per
+    rank (the pages' low-precision threshold), L2 flushed before each call."""
+    import precision_collective_reduction_gb300 as pcr
+    w = W.LP_FLAT_N8_16MB_BF16
+    N, n = w.nranks, w.n
+    host = W.draw_all(w)
+    ins = []
+    for h in host:
+        ins.append(torch.from_numpy(h).view(torch.int16).view(torch.bfloat16).cuda())
+    nb = pcr.nblocks(n)
+    wc = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(N)]
+    ws = [torch.empty(N * nb, dtype=torch.float32, device="cuda") for _ in range(N)]
+    scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    per = pcr.shard_len(n, N)
+    rs_out = [torch.empty(max(1, min(per, n - r * per)), dtype=torch.bfloat16,
+                          device="cuda") for r in range(N)]
+    m = n // N
+    ag_in = [t[:m] for t in ins]
+    full_out = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+    calls = {
+        "reduce_scatter": (lambda s: pcr.reduce_scatter_sim(
+            ins, rs_out, wire_codes=wc, wire_scales=ws, stream=s), n),
+        "all_gather": (lambda s: pcr.all_gather_sim(
+            ag_in, full_out, wire_codes=wc, wire_scales=ws, stream=s), m),
+        "all_to_all": (lambda s: pcr.all_to_all_sim(
+            ins, full_out, wire_codes=wc, wire_scales=ws, stream=s), n // N),
+    }
+    out = {}
+    for kind, (fn, count) in calls.items():
+        for _ in range(3):
+            fn(stream)
+        times = []
+        with torch.cuda.stream(stream):
+            for _ in range(iters):
+                flush_l2(torch, scratch)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn(stream)
+                b.record(stream)
+                b.synchronize()
+                times.append(a.elapsed_time(b) * 1e3)
+        us = statistics.median(times)
+        nbytes = collective_bytes(kind, N, count, 2, 128)
+        out[kind] = {"us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
+                     "bytes_alg": nbytes, "count_per_rank": count, "l2": "flushed"}
+    del ins, wc, ws, scratch, rs_out, full_out
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -444,6 +509,7 @@ def run_ours(args):
             wl.name: measure_small(torch, wl, stream, iters=20)
             for wl in (W.LP_FLAT_N2_1M_F32, W.LP_FLAT_N8_16MB_BF16,
                        W.LP_TREE_N8_64MB_BF16)}
+        extras["collectives_lp_n8_16MiB_bf16"] = measure_collectives(torch, stream)
     clocks.stop()
 
     if rank != 0:

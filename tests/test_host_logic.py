@@ -58,3 +58,13 @@ def test_workload_recipes():
     a = W.draw(W.LP_FLAT_N2_1M_F32, 1, n=1000)
     assert np.array_equal(a, W.draw(W.LP_FLAT_N2_1M_F32, 1, n=1000))   # seeded
     assert not np.array_equal(a, W.draw(W.LP_FLAT_N2_1M_F32, 0, n=1000))
+
+
+def test_collective_bytes():
+    n, N = 8 * MiB, 8
+    q = n + 4 * (n // 128)
+    assert bench.collective_bytes("reduce_scatter", N, n, 2, 128) == N * n * 2 + N * q + n * 2
+    m = n // N
+    assert bench.collective_bytes("all_gather", N, m, 2, 128) == \
+        N * m * 2 + N * (m + 4 * m // 128) + N * N * m * 2
+    assert bench.collective_bytes("all_to_all", N, m, 2, 0) == 2 * N * N * m * 2
