@@ -1,13 +1,14 @@
 // lpcoll_gather.cu -- the collectives without a reduction: AllGather and
 // AlltoAll over N emulated ranks, exact or low precision.
 //
-// Each warp takes one unit (32 x kVec elements) of one sender's data: it
-// loads it, and in low precision quantizes it on the sender's blocks (one
-// absmax scale per 128 elements counted from the start of what the sender
-// sends), stores the codes and scales to the sender's wire payload, and
-// dequantizes them in registers; then it writes the (dequantized) values to
-// the receiving outputs. Warps stride over (sender, destination, unit)
-// items, so each sender's data streams through HBM in order.
+// Each warp takes an item of kItemUnits consecutive units (32 x kVec
+// elements each) of one sender's data: it loads them all, and in low
+// precision quantizes them on the sender's blocks (one absmax scale per 128
+// elements counted from the start of what the sender sends), stores the
+// codes and scales to the sender's wire payload, and dequantizes them in
+// registers; then it writes the (dequantized) values to the receiving
+// outputs. Warps stride over (sender, destination, item), so each sender's
+// data streams through HBM in order.
 //
 // Offsets that are not 16-byte aligned (a contribution or chunk length that
 // is not a multiple of 16 bytes) take the element-by-element path for the
@@ -25,128 +26,159 @@ __device__ __forceinline__ int access_count(int cnt, bool aligned)
     return (aligned || cnt != Fmt<DT>::kVec) ? cnt : -cnt;
 }
 
-// One unit of sender r's contribution (m elements) to the AllGather.
-template <int DT, bool LP, bool ALIGNED, bool FULL>
-__device__ __forceinline__ void gather_unit(const DdaParams &p, int nranks, size_t m,
-                                            int r, size_t u, int lane)
+// Units per work item: a warp loads kItemUnits consecutive units of one
+// sender before processing them, so each lane keeps kItemUnits 16-byte loads
+// in flight (one sender per item would leave the loop latency-bound).
+constexpr int kItemUnits = 8;
+
+// Quantize-dequantize (LP) or pass through the kItemUnits vectors of one
+// item, whose lane offsets are e0[k] with cnt[k] valid elements; x receives
+// the values to deliver.
+template <int DT, bool LP>
+__device__ __forceinline__ void encode_item(const DdaParams &p, int r, size_t code_base,
+                                            size_t scale_base,
+                                            const size_t (&e0)[kItemUnits],
+                                            const int (&cnt)[kItemUnits],
+                                            const uint4 (&raw)[kItemUnits], bool aligned,
+                                            int lane, float (&x)[kItemUnits][Fmt<DT>::kVec])
+{
+#pragma unroll
+    for (int k = 0; k < kItemUnits; ++k) {
+        widen<DT>(raw[k], x[k]);
+        if constexpr (LP) {
+            float s;
+            const Codes<DT> c = quantize_lane<DT>(x[k], s);
+            if (cnt[k] > 0) {
+                store_codes(p.codes[r], code_base + e0[k], access_count<DT>(cnt[k], aligned),
+                            c);
+                if ((lane % Fmt<DT>::kGroup) == 0)
+                    __stcs(p.scales[r] + scale_base + e0[k] / kBlock, s);
+            }
+            dequantize_lane<DT>(c, s, x[k]);
+        }
+    }
+}
+
+// One item of sender r's contribution (m elements) to the AllGather:
+// units [g kItemUnits, (g+1) kItemUnits).
+template <int DT, bool LP, bool ALIGNED>
+__device__ __forceinline__ void gather_item(const DdaParams &p, int nranks, size_t m,
+                                            int r, size_t g, int lane)
 {
     constexpr int V = Fmt<DT>::kVec;
-    const size_t e0 = (u * 32 + lane) * V;
-    const int cnt = FULL ? V : lane_count<DT>(m, e0);
-    const uint4 raw = (FULL || cnt > 0) ? load_vec<DT>(p.in[r], e0, cnt)
-                                        : make_uint4(0u, 0u, 0u, 0u);
-    float x[V];
-    widen<DT>(raw, x);
-    if constexpr (LP) {
-        float s;
-        const Codes<DT> c = quantize_lane<DT>(x, s);
-        if (FULL || cnt > 0) {
-            store_codes(p.codes[r], e0, cnt, c);
-            if ((lane % Fmt<DT>::kGroup) == 0)
-                __stcs(p.scales[r] + e0 / kBlock, s);
-        }
-        dequantize_lane<DT>(c, s, x);
+    size_t e0[kItemUnits];
+    int cnt[kItemUnits];
+    uint4 raw[kItemUnits];
+#pragma unroll
+    for (int k = 0; k < kItemUnits; ++k) {
+        e0[k] = ((g * kItemUnits + k) * 32 + lane) * V;
+        cnt[k] = lane_count<DT>(m, e0[k]);
+        raw[k] = cnt[k] > 0 ? load_vec<DT>(p.in[r], e0[k], cnt[k]) : make_uint4(0u, 0u, 0u, 0u);
     }
-    if (FULL || cnt > 0) {
-        const uint4 o = narrow<DT>(x);
-        const size_t at = static_cast<size_t>(r) * m + e0;
-        const int k = access_count<DT>(cnt, ALIGNED);
-        for (int d = 0; d < nranks; ++d)
-            store_vec<DT>(p.out[d], at, k, o);
+    float x[kItemUnits][V];
+    encode_item<DT, LP>(p, r, 0, 0, e0, cnt, raw, true, lane, x);
+    const size_t at = static_cast<size_t>(r) * m;
+#pragma unroll
+    for (int k = 0; k < kItemUnits; ++k) {
+        if (cnt[k] > 0) {
+            const uint4 o = narrow<DT>(x[k]);
+            const int a = access_count<DT>(cnt[k], ALIGNED);
+            for (int d = 0; d < nranks; ++d)
+                store_vec<DT>(p.out[d], at + e0[k], a, o);
+        }
     }
 }
 
 template <int DT, bool LP, bool ALIGNED>
 __global__ void __launch_bounds__(kThreads)
-gather_kernel(const __grid_constant__ DdaParams p, int nranks, size_t m,
-              size_t units, size_t full_units)
+gather_kernel(const __grid_constant__ DdaParams p, int nranks, size_t m, size_t groups)
 {
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
-    const size_t items = static_cast<size_t>(nranks) * units;
+    const size_t items = static_cast<size_t>(nranks) * groups;
     for (size_t it = warp; it < items; it += nwarps) {
-        const int r = static_cast<int>(it / units);
-        const size_t u = it - static_cast<size_t>(r) * units;
-        if (u < full_units)
-            gather_unit<DT, LP, ALIGNED, true>(p, nranks, m, r, u, lane);
-        else
-            gather_unit<DT, LP, ALIGNED, false>(p, nranks, m, r, u, lane);
+        const int r = static_cast<int>(it / groups);
+        gather_item<DT, LP, ALIGNED>(p, nranks, m, r, it - static_cast<size_t>(r) * groups,
+                                     lane);
     }
 }
 
-// One unit of chunk j (c elements) of sender r in the AlltoAll.
-template <int DT, bool LP, bool ALIGNED, bool FULL>
-__device__ __forceinline__ void alltoall_unit(const DdaParams &p, size_t c, size_t nbc,
-                                              int r, int j, size_t u, int lane)
+// One item of chunk j (c elements) of sender r in the AlltoAll.
+template <int DT, bool LP, bool ALIGNED>
+__device__ __forceinline__ void alltoall_item(const DdaParams &p, size_t c, size_t nbc,
+                                              int r, int j, size_t g, int lane)
 {
     constexpr int V = Fmt<DT>::kVec;
-    const size_t e0 = (u * 32 + lane) * V;
-    const int cnt = FULL ? V : lane_count<DT>(c, e0);
-    const int k = access_count<DT>(cnt, ALIGNED);
-    const size_t src = static_cast<size_t>(j) * c + e0;
-    const uint4 raw = (FULL || cnt > 0) ? load_vec<DT>(p.in[r], src, k)
-                                        : make_uint4(0u, 0u, 0u, 0u);
-    float x[V];
-    widen<DT>(raw, x);
-    if constexpr (LP) {
-        float s;
-        const Codes<DT> cd = quantize_lane<DT>(x, s);
-        if (FULL || cnt > 0) {
-            store_codes(p.codes[r], src, k, cd);
-            if ((lane % Fmt<DT>::kGroup) == 0)
-                __stcs(p.scales[r] + static_cast<size_t>(j) * nbc + e0 / kBlock, s);
-        }
-        dequantize_lane<DT>(cd, s, x);
+    const size_t src = static_cast<size_t>(j) * c;
+    size_t e0[kItemUnits];
+    int cnt[kItemUnits];
+    uint4 raw[kItemUnits];
+#pragma unroll
+    for (int k = 0; k < kItemUnits; ++k) {
+        e0[k] = ((g * kItemUnits + k) * 32 + lane) * V;
+        cnt[k] = lane_count<DT>(c, e0[k]);
+        raw[k] = cnt[k] > 0 ? load_vec<DT>(p.in[r], src + e0[k], access_count<DT>(cnt[k], ALIGNED))
+                            : make_uint4(0u, 0u, 0u, 0u);
     }
-    if (FULL || cnt > 0)
-        store_vec<DT>(p.out[j], static_cast<size_t>(r) * c + e0, k, narrow<DT>(x));
+    float x[kItemUnits][V];
+    encode_item<DT, LP>(p, r, src, static_cast<size_t>(j) * nbc, e0, cnt, raw, ALIGNED,
+                        lane, x);
+    const size_t at = static_cast<size_t>(r) * c;
+#pragma unroll
+    for (int k = 0; k < kItemUnits; ++k)
+        if (cnt[k] > 0)
+            store_vec<DT>(p.out[j], at + e0[k], access_count<DT>(cnt[k], ALIGNED),
+                          narrow<DT>(x[k]));
 }
 
 template <int DT, bool LP, bool ALIGNED>
 __global__ void __launch_bounds__(kThreads)
 alltoall_kernel(const __grid_constant__ DdaParams p, int nranks, size_t c, size_t nbc,
-                size_t units, size_t full_units)
+                size_t groups)
 {
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
-    const size_t per_sender = static_cast<size_t>(nranks) * units;
+    const size_t per_sender = static_cast<size_t>(nranks) * groups;
     const size_t items = static_cast<size_t>(nranks) * per_sender;
     for (size_t it = warp; it < items; it += nwarps) {
         const int r = static_cast<int>(it / per_sender);
         const size_t rest = it - static_cast<size_t>(r) * per_sender;
-        const int j = static_cast<int>(rest / units);
-        const size_t u = rest - static_cast<size_t>(j) * units;
-        if (u < full_units)
-            alltoall_unit<DT, LP, ALIGNED, true>(p, c, nbc, r, j, u, lane);
-        else
-            alltoall_unit<DT, LP, ALIGNED, false>(p, c, nbc, r, j, u, lane);
+        const int j = static_cast<int>(rest / groups);
+        alltoall_item<DT, LP, ALIGNED>(p, c, nbc, r, j, rest - static_cast<size_t>(j) * groups,
+                                       lane);
     }
+}
+
+// Items of kItemUnits units covering a length of `len` elements.
+template <int DT>
+inline size_t item_groups(size_t len)
+{
+    size_t full, units;
+    unit_counts<DT>(len, full, units);
+    return (units + kItemUnits - 1) / kItemUnits;
 }
 
 template <int DT, bool LP, bool ALIGNED>
 cudaError_t launch_gather_t(const DdaParams &p, int nranks, size_t m, cudaStream_t st)
 {
-    size_t full, units;
-    unit_counts<DT>(m, full, units);
+    const size_t groups = item_groups<DT>(m);
     const void *k = reinterpret_cast<const void *>(&gather_kernel<DT, LP, ALIGNED>);
-    const int grid = wave_ctas(k, units * static_cast<size_t>(nranks));
-    gather_kernel<DT, LP, ALIGNED><<<grid, kThreads, 0, st>>>(p, nranks, m, units, full);
+    const int grid = wave_ctas(k, groups * static_cast<size_t>(nranks));
+    gather_kernel<DT, LP, ALIGNED><<<grid, kThreads, 0, st>>>(p, nranks, m, groups);
     return cudaGetLastError();
 }
 
 template <int DT, bool LP, bool ALIGNED>
 cudaError_t launch_alltoall_t(const DdaParams &p, int nranks, size_t c, cudaStream_t st)
 {
-    size_t full, units;
-    unit_counts<DT>(c, full, units);
+    const size_t groups = item_groups<DT>(c);
     const size_t nbc = (c + kBlock - 1) / kBlock;
     const void *k = reinterpret_cast<const void *>(&alltoall_kernel<DT, LP, ALIGNED>);
     const int grid =
-        wave_ctas(k, units * static_cast<size_t>(nranks) * static_cast<size_t>(nranks));
-    alltoall_kernel<DT, LP, ALIGNED><<<grid, kThreads, 0, st>>>(p, nranks, c, nbc, units,
-                                                                 full);
+        wave_ctas(k, groups * static_cast<size_t>(nranks) * static_cast<size_t>(nranks));
+    alltoall_kernel<DT, LP, ALIGNED><<<grid, kThreads, 0, st>>>(p, nranks, c, nbc, groups);
     return cudaGetLastError();
 }
 
