@@ -56,23 +56,36 @@ __device__ __forceinline__ void scatter_store(const DdaParams &p, size_t e0, int
     }
 }
 
+// Units a warp takes per loop iteration: enough that each lane keeps about
+// eight 16-byte loads in flight (N loads per unit) whatever the rank count.
+template <int N>
+__host__ __device__ constexpr int units_per_iter()
+{
+    return N >= 8 ? 1 : (N >= 4 ? 2 : (N >= 2 ? 4 : 8));
+}
+
+// Loads of one unit: the N ranks' 16-byte vectors of this lane.
+template <int N, int DT, bool FULL>
+__device__ __forceinline__ void load_unit(const DdaParams &p, size_t e0, int cnt,
+                                          uint4 (&raw)[N])
+{
+#pragma unroll
+    for (int r = 0; r < N; ++r)
+        raw[r] = (FULL || cnt > 0) ? load_vec<DT>(p.in[r], e0, cnt)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Everything after the loads: quantize / dequantize / reduce / requantize,
+// then the output stores.
 template <int N, int DT, int MODE, bool FULL>
-__device__ __forceinline__ void dda_unit(const DdaParams &p, size_t n, size_t unit,
-                                         int lane)
+__device__ __forceinline__ void process_unit(const DdaParams &p, size_t e0, int cnt,
+                                             int lane, const uint4 (&raw)[N])
 {
     using F = Fmt<DT>;
     constexpr int V = F::kVec;
     constexpr bool kExactSum = (MODE == kExact || MODE == kScatterExact);
     constexpr bool kScatter = (MODE == kScatterExact || MODE == kScatterLp);
-    const size_t e0 = (unit * 32 + lane) * V;
-    const int cnt = FULL ? V : lane_count<DT>(n, e0);
     const bool leader = (lane % F::kGroup) == 0;
-
-    uint4 raw[N];
-#pragma unroll
-    for (int r = 0; r < N; ++r)
-        raw[r] = (FULL || cnt > 0) ? load_vec<DT>(p.in[r], e0, cnt)
-                                   : make_uint4(0u, 0u, 0u, 0u);
 
     float acc[V];
 #pragma unroll
@@ -122,15 +135,50 @@ __device__ __forceinline__ void dda_unit(const DdaParams &p, size_t n, size_t un
     }
 }
 
+template <int N, int DT, int MODE, bool FULL>
+__device__ __forceinline__ void dda_unit(const DdaParams &p, size_t n, size_t unit,
+                                         int lane)
+{
+    constexpr int V = Fmt<DT>::kVec;
+    const size_t e0 = (unit * 32 + lane) * V;
+    const int cnt = FULL ? V : lane_count<DT>(n, e0);
+    uint4 raw[N];
+    load_unit<N, DT, FULL>(p, e0, cnt, raw);
+    process_unit<N, DT, MODE, FULL>(p, e0, cnt, lane, raw);
+}
+
+// K consecutive full units, all K x N loads issued before any processing.
+template <int N, int DT, int MODE, int K>
+__device__ __forceinline__ void dda_units(const DdaParams &p, size_t unit0, int lane)
+{
+    constexpr int V = Fmt<DT>::kVec;
+    uint4 raw[K][N];
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+        load_unit<N, DT, true>(p, ((unit0 + k) * 32 + lane) * V, V, raw[k]);
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+        process_unit<N, DT, MODE, true>(p, ((unit0 + k) * 32 + lane) * V, V, lane, raw[k]);
+}
+
 template <int N, int DT, int MODE>
 __global__ void __launch_bounds__(kThreads)
 dda_kernel(const __grid_constant__ DdaParams p, size_t n, size_t full_units,
            size_t total_units)
 {
+    constexpr int K = units_per_iter<N>();
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
-    for (size_t u = warp; u < full_units; u += nwarps)
+    size_t u = warp;
+    if constexpr (K > 1) {
+        // groups of K consecutive units, then the full units left over
+        const size_t groups = full_units / K;
+        for (size_t g = warp; g < groups; g += nwarps)
+            dda_units<N, DT, MODE, K>(p, g * K, lane);
+        u = groups * K + warp;
+    }
+    for (; u < full_units; u += nwarps)
         dda_unit<N, DT, MODE, true>(p, n, u, lane);
     // the ragged last unit (at most one) goes to the warp that would take it
     if (total_units > full_units && warp == full_units % nwarps)
@@ -156,7 +204,8 @@ cudaError_t launch_dda_n(const DdaParams &p, size_t n, cudaStream_t stream)
     size_t full, total;
     unit_counts<DT>(n, full, total);
     const void *k = reinterpret_cast<const void *>(&dda_kernel<N, DT, MODE>);
-    const int grid = wave_ctas(k, total);
+    const size_t K = units_per_iter<N>();
+    const int grid = wave_ctas(k, (total + K - 1) / K);
     dda_kernel<N, DT, MODE><<<grid, kThreads, 0, stream>>>(p, n, full, total);
     return cudaGetLastError();
 }
