@@ -536,6 +536,46 @@ def run_ours(args):
     return 0
 
 
+def run_crossover(args):
+    """Flat vs tree allreduce time across message sizes (8 ranks, BF16, exact
+    and low precision, L2 flushed before every call): one JSON line per size."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from precision_collective_reduction_gb300 import runner
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    N = 8
+    for kib in (8, 32, 128, 512, 2048, 8192, 32768, 131072):
+        n = kib * 1024 // 2
+        row = {"nranks": N, "message_KiB": kib, "dtype": "bf16"}
+        for block in (0, 128):
+            bufs = runner.RankBuffers(N, n, W.BF16, block, separate_tree_out=True)
+            bufs.load(W.random_inputs(N, n, W.BF16, 5, scale_spread=1.0))
+            s = stream.cuda_stream
+            for algo in ("flat", "tree"):
+                for _ in range(3):
+                    bufs.run(algo, s)
+                times = []
+                with torch.cuda.stream(stream):
+                    for _ in range(args.steps):
+                        flush_l2(torch, scratch)
+                        a = torch.cuda.Event(enable_timing=True)
+                        b = torch.cuda.Event(enable_timing=True)
+                        a.record(stream)
+                        bufs.run(algo, s)
+                        b.record(stream)
+                        b.synchronize()
+                        times.append(a.elapsed_time(b) * 1e3)
+                key = "%s_%s_us" % ("lp" if block else "exact", algo)
+                row[key] = round(statistics.median(times), 3)
+            del bufs
+            torch.cuda.empty_cache()
+        print(json.dumps(row), flush=True)
+    return 0
+
+
 def run_profile_case(args):
     """A few launches of one workload's kernels, for ncu captures: `warmup`
     untimed launches of each algorithm, then `steps` more."""
@@ -575,9 +615,13 @@ def main():
     ap.add_argument("--elems", type=int, default=0,
                     help="with --profile-case: elements per rank (default: full)")
     ap.add_argument("--algo", choices=["flat", "tree"], default=None)
+    ap.add_argument("--crossover", action="store_true",
+                    help="only time flat vs tree over message sizes")
     args = ap.parse_args()
     if args.profile_case:
         return run_profile_case(args)
+    if args.crossover:
+        return run_crossover(args)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
