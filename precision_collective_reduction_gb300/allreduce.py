@@ -10,8 +10,8 @@ Algorithm choice (host logic only; the work runs in liblpcoll's kernels):
 - Even when asked for, it applies only to messages of at least
   ``LPCOLL_LP_MIN_BYTES`` bytes (default 16 MiB, the pages' threshold for the
   low-precision collectives); smaller messages are reduced exactly.
-- ``algo``: "flat", "tree", or "auto". The pages say only that tree is for
-  "slightly larger" messages. Measured on one GB300 with 8 emulated ranks
+- ``algo``: "flat", "tree", or "auto". The pages place tree at
+  somewhat larger messages than flat. Measured on one GB300 with 8 emulated ranks
   (BF16, 8 KiB to 128 MiB per rank), flat is never slower than tree: the
   exact tree is the same kernel, and the low-precision tree adds a
   requantization and a shard wire (3-16% slower from 2 MiB up). So "auto"
