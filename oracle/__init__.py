@@ -18,6 +18,8 @@ from . import build as _build
 F32 = 0
 BF16 = 1
 BLOCK = 128
+E4M3 = 0
+E5M2 = 1
 
 _lib = None
 
@@ -50,6 +52,22 @@ def _load(path):
     for f in ("orc_reduce_scatter", "orc_all_gather", "orc_all_to_all"):
         getattr(L, f).argtypes = [pp, pp, ctypes.c_int, c_sz, ctypes.c_int,
                                   ctypes.c_int, pp, pp]
+        getattr(L, f).restype = ctypes.c_int
+    L.orc_e5m2_decode.argtypes = [ctypes.c_uint8]
+    L.orc_e5m2_decode.restype = ctypes.c_float
+    L.orc_e5m2_encode.argtypes = [ctypes.c_float]
+    L.orc_e5m2_encode.restype = ctypes.c_uint8
+    L.orc_block_scale_fmt.argtypes = [ctypes.c_float, ctypes.c_int,
+                                      ctypes.POINTER(ctypes.c_float),
+                                      ctypes.POINTER(ctypes.c_float)]
+    L.orc_block_scale_fmt.restype = None
+    L.orc_quantize_fmt.argtypes = [vp, ctypes.c_int, c_sz, ctypes.c_int,
+                                   ctypes.c_int, vp, vp]
+    L.orc_dequantize_fmt.argtypes = [vp, vp, c_sz, ctypes.c_int, ctypes.c_int,
+                                     vp, ctypes.c_int]
+    L.orc_reduce_fmt.argtypes = [pp, pp, ctypes.c_int, c_sz, ctypes.c_int,
+                                 ctypes.c_int, vp, ctypes.c_int]
+    for f in ("orc_quantize_fmt", "orc_dequantize_fmt", "orc_reduce_fmt"):
         getattr(L, f).restype = ctypes.c_int
     L.orc_shard_len.argtypes = [c_sz, ctypes.c_int, ctypes.c_int]
     L.orc_shard_len.restype = c_sz
@@ -302,6 +320,63 @@ def all_to_all(inputs, block=BLOCK):
         wc = [x[:nranks * c] for x in wc]
         ws = [x[:nranks * nblocks(c, block)] for x in ws]
     return outs, wc, ws
+
+
+# -- format / block-size variants ---------------------------------------------
+
+def e5m2_decode(code):
+    return lib().orc_e5m2_decode(int(code))
+
+
+def e5m2_encode(y):
+    return lib().orc_e5m2_encode(float(y))
+
+
+def e5m2_decode_all():
+    return np.array([e5m2_decode(c) for c in range(256)], dtype=np.float32)
+
+
+def e5m2_encode_array(y):
+    y = np.ascontiguousarray(y, dtype=np.float32).ravel()
+    L = lib()
+    return np.fromiter((L.orc_e5m2_encode(float(v)) for v in y), dtype=np.uint8,
+                       count=y.size)
+
+
+def block_scale_fmt(amax, fmt):
+    s = ctypes.c_float()
+    inv = ctypes.c_float()
+    lib().orc_block_scale_fmt(float(amax), int(fmt), ctypes.byref(s), ctypes.byref(inv))
+    return np.float32(s.value), np.float32(inv.value)
+
+
+def quantize_fmt(x, block, fmt):
+    x = np.ascontiguousarray(x)
+    n = x.size
+    codes = np.zeros(max(n, 1), dtype=np.uint8)
+    scales = np.zeros(max(nblocks(n, block), 1), dtype=np.float32)
+    _check(lib().orc_quantize_fmt(_ptr(x), _dtype_code(x), n, block, fmt, _ptr(codes),
+                                  _ptr(scales)), "quantize_fmt")
+    return codes[:n], scales[:nblocks(n, block)]
+
+
+def dequantize_fmt(codes, scales, block, fmt, dtype=np.float32):
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    out = np.zeros(max(codes.size, 1), dtype=dtype)
+    _check(lib().orc_dequantize_fmt(_ptr(codes), _ptr(scales), codes.size, block, fmt,
+                                    _ptr(out), _dtype_code(out)), "dequantize_fmt")
+    return out[:codes.size]
+
+
+def reduce_fmt(codes_list, scales_list, block, fmt, dtype=np.float32):
+    codes_list = [np.ascontiguousarray(c, dtype=np.uint8) for c in codes_list]
+    scales_list = [np.ascontiguousarray(s, dtype=np.float32) for s in scales_list]
+    n = codes_list[0].size
+    out = np.zeros(max(n, 1), dtype=dtype)
+    _check(lib().orc_reduce_fmt(_ptrs(codes_list), _ptrs(scales_list), len(codes_list),
+                                n, block, fmt, _ptr(out), _dtype_code(out)), "reduce_fmt")
+    return out[:n]
 
 
 def shard_len(n, nranks, block=BLOCK):

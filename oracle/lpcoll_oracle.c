@@ -119,6 +119,57 @@ uint8_t orc_e4m3_encode(float y)
     return sign | (uint8_t)(((e + 7) << 3) | ((int)m - 8));
 }
 
+/* Value of an OCP E5M2 code: sign bit, 5 exponent bits (bias 15), 2 mantissa
+ * bits. Exponent field 0 holds subnormals M * 2^-16; exponent field 31 holds
+ * +-Inf (M = 0) and NaN (M != 0). Every value is exact in binary32. */
+float orc_e5m2_decode(uint8_t c)
+{
+    int sign = c >> 7;
+    int e = (c >> 2) & 31;
+    int m = c & 3;
+    double v;
+    if (e == 31)
+        return m ? NAN : (sign ? -INFINITY : INFINITY);
+    if (e == 0)
+        v = ldexp((double)m, -16);
+    else
+        v = ldexp((double)(4 + m), e - 17); /* (1 + m/4) * 2^(e-15) */
+    return (float)(sign ? -v : v);
+}
+
+/* Nearest E5M2 code to y, ties to the even code; magnitudes beyond the
+ * largest finite value 57344 (Inf included) give +-57344 (satfinite); NaN
+ * gives 0x7F; the sign of zero is kept. Same one-rounding construction as
+ * the E4M3 encoder. */
+uint8_t orc_e5m2_encode(float y)
+{
+    uint32_t bits;
+    uint8_t sign;
+    double a, m;
+    int k, e;
+
+    memcpy(&bits, &y, sizeof bits);
+    sign = (bits >> 31) ? 0x80 : 0x00;
+    if (isnan(y))
+        return 0x7F;
+    a = fabs((double)y);
+    if (a > 57344.0)
+        return sign | 0x7B;
+    if (a < 0x1p-14) {
+        /* subnormal spacing 2^-16; m == 4 is the smallest normal (code 4) */
+        m = nearbyint(a * 0x1p16);
+        return sign | (uint8_t)m;
+    }
+    frexp(a, &k);
+    e = k - 1;                      /* -14 .. 15 */
+    m = nearbyint(ldexp(a, 2 - e)); /* 4 .. 8 */
+    if (m == 8.0) {
+        e += 1;
+        m = 4.0;
+    }
+    return sign | (uint8_t)(((e + 15) << 2) | ((int)m - 4));
+}
+
 float orc_bf16_to_f32(uint16_t h)
 {
     uint32_t u = (uint32_t)h << 16;
@@ -160,48 +211,94 @@ static void store_elem(void *buf, int dtype, size_t i, float v)
 /* Scale of a block whose largest magnitude is amax. Writes s (kept in the
  * payload) and inv (the multiplier applied to each element). Both are single
  * IEEE divisions. */
-void orc_block_scale(float amax, float *s, float *inv)
+#define ORC_E4M3 0
+#define ORC_E5M2 1
+
+/* Largest finite value of the FP8 format: the value the block maximum maps to. */
+static float fp8_max(int fmt)
 {
-    float q = 448.0f / amax;
+    return fmt == ORC_E5M2 ? 57344.0f : 448.0f;
+}
+
+static uint8_t fp8_encode(int fmt, float y)
+{
+    return fmt == ORC_E5M2 ? orc_e5m2_encode(y) : orc_e4m3_encode(y);
+}
+
+static float fp8_decode(int fmt, uint8_t c)
+{
+    return fmt == ORC_E5M2 ? orc_e5m2_decode(c) : orc_e4m3_decode(c);
+}
+
+/* Scale of a block whose largest magnitude is amax, for format fmt: s =
+ * amax / max (kept in the payload) and inv = max / amax (the multiplier
+ * applied to each element), each one IEEE division; a block whose inv
+ * overflows gets s = inv = 0. */
+void orc_block_scale_fmt(float amax, int fmt, float *s, float *inv)
+{
+    float q = fp8_max(fmt) / amax;
     if (isinf(q)) {
         *s = 0.0f;
         *inv = 0.0f;
         return;
     }
-    *s = amax / 448.0f;
+    *s = amax / fp8_max(fmt);
     *inv = q;
 }
 
+void orc_block_scale(float amax, float *s, float *inv)
+{
+    orc_block_scale_fmt(amax, ORC_E4M3, s, inv);
+}
+
 /* Quantize values v[0..len) (one block) into codes[0..len) and return s. */
-static float quantize_block(const float *v, size_t len, uint8_t *codes)
+static float quantize_block_fmt(const float *v, size_t len, uint8_t *codes, int fmt)
 {
     float amax = 0.0f, s, inv;
     size_t i;
     for (i = 0; i < len; i++)
         amax = fmaxf(amax, fabsf(v[i]));
-    orc_block_scale(amax, &s, &inv);
+    orc_block_scale_fmt(amax, fmt, &s, &inv);
     for (i = 0; i < len; i++) {
         if (inv == 0.0f) {
             codes[i] = signbit(v[i]) ? 0x80 : 0x00;
         } else {
             float y = v[i] * inv;
-            codes[i] = orc_e4m3_encode(y);
+            codes[i] = fp8_encode(fmt, y);
         }
     }
     return s;
 }
 
+static float quantize_block(const float *v, size_t len, uint8_t *codes)
+{
+    return quantize_block_fmt(v, len, codes, ORC_E4M3);
+}
+
+static float dequant_elem_fmt(const uint8_t *codes, const float *scales,
+                              int block, size_t i, int fmt)
+{
+    float d = fp8_decode(fmt, codes[i]);
+    float s = scales[i / (size_t)block];
+    return d * s;
+}
+
 static float dequant_elem(const uint8_t *codes, const float *scales,
                           int block, size_t i)
 {
-    float d = orc_e4m3_decode(codes[i]);
-    float s = scales[i / (size_t)block];
-    return d * s;
+    return dequant_elem_fmt(codes, scales, block, i, ORC_E4M3);
 }
 
 static int check_block(int block)
 {
     return block == 128 ? ORC_OK : ORC_ERR_UNSUPPORTED;
+}
+
+/* Block sizes of the format / block-size variants. */
+static int check_block_variant(int block)
+{
+    return (block == 32 || block == 64 || block == 128 || block == 256)
+               ? ORC_OK : ORC_ERR_UNSUPPORTED;
 }
 
 static int check_dtype(int dtype)
@@ -530,5 +627,63 @@ int orc_all_to_all(const void *const *in, void *const *out, int nranks, size_t c
                                 : load_elem(in[r], dtype, (size_t)j * c + i);
                 store_elem(out[j], dtype, (size_t)r * c + i, v);
             }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Format and block-size variants of the staged building blocks (an          */
+/* ablation: the pages fix neither the FP8 format nor the block). fmt is     */
+/* ORC_E4M3 or ORC_E5M2; block is 32, 64, 128 or 256. With fmt = ORC_E4M3     */
+/* and block = 128 they equal orc_quantize / orc_dequantize / orc_reduce.    */
+/* ------------------------------------------------------------------------ */
+
+int orc_quantize_fmt(const void *in, int dtype, size_t n, int block, int fmt,
+                     uint8_t *codes, float *scales)
+{
+    float buf[256];
+    size_t b, nb, lo, len, i;
+    if (check_dtype(dtype) || (fmt != ORC_E4M3 && fmt != ORC_E5M2))
+        return ORC_ERR_ARG;
+    if (check_block_variant(block))
+        return ORC_ERR_UNSUPPORTED;
+    nb = (n + (size_t)block - 1) / (size_t)block;
+    for (b = 0; b < nb; b++) {
+        lo = b * (size_t)block;
+        len = (n - lo < (size_t)block) ? n - lo : (size_t)block;
+        for (i = 0; i < len; i++)
+            buf[i] = load_elem(in, dtype, lo + i);
+        scales[b] = quantize_block_fmt(buf, len, codes + lo, fmt);
+    }
+    return ORC_OK;
+}
+
+int orc_dequantize_fmt(const uint8_t *codes, const float *scales, size_t n,
+                       int block, int fmt, void *out, int dtype)
+{
+    size_t i;
+    if (check_dtype(dtype) || (fmt != ORC_E4M3 && fmt != ORC_E5M2))
+        return ORC_ERR_ARG;
+    if (check_block_variant(block))
+        return ORC_ERR_UNSUPPORTED;
+    for (i = 0; i < n; i++)
+        store_elem(out, dtype, i, dequant_elem_fmt(codes, scales, block, i, fmt));
+    return ORC_OK;
+}
+
+int orc_reduce_fmt(const uint8_t *const *codes, const float *const *scales,
+                   int nranks, size_t n, int block, int fmt, void *out, int dtype)
+{
+    size_t i;
+    int r;
+    if (nranks < 1 || check_dtype(dtype) || (fmt != ORC_E4M3 && fmt != ORC_E5M2))
+        return ORC_ERR_ARG;
+    if (check_block_variant(block))
+        return ORC_ERR_UNSUPPORTED;
+    for (i = 0; i < n; i++) {
+        float sum = dequant_elem_fmt(codes[0], scales[0], block, i, fmt);
+        for (r = 1; r < nranks; r++)
+            sum = sum + dequant_elem_fmt(codes[r], scales[r], block, i, fmt);
+        store_elem(out, dtype, i, sum);
+    }
     return ORC_OK;
 }

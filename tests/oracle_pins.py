@@ -601,4 +601,145 @@ def pin_all_to_all(oracle):
                 assert np.all(np.abs(got - T) <= bound)
 
 
+# -- format and block-size variants (E5M2; blocks of 32, 64, 128, 256) --------
+
+E4M3, E5M2 = 0, 1
+FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
+VARIANT_BLOCKS = (32, 64, 128, 256)
+
+
+def torch_e5m2_table():
+    return (torch.arange(256, dtype=torch.uint8).view(torch.float8_e5m2)
+            .float().numpy())
+
+
+def torch_e5m2_encode(y):
+    """PyTorch's RNE float32 -> e5m2 (valid for |y| <= 57344)."""
+    t = torch.from_numpy(np.ascontiguousarray(y, dtype=np.float32))
+    return t.to(torch.float8_e5m2).view(torch.uint8).numpy()
+
+
+def pin_e5m2_decode(oracle):
+    ours = oracle.e5m2_decode_all()
+    ref = torch_e5m2_table()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert same_bits(ours[~nan], ref[~nan])
+    # spec points: max finite 1.75 * 2^15, min normal 2^-14, min subnormal
+    # 2^-16, +-Inf at S.11111.00
+    assert ours[0x7B] == 57344.0 and ours[0x04] == 2.0 ** -14
+    assert ours[0x01] == 2.0 ** -16 and ours[0x7C] == np.inf and ours[0xFC] == -np.inf
+    pos = ours[:0x7C].astype(np.float64)
+    gaps = np.diff(pos)
+    assert np.all(gaps > 0)
+    spacing = [gaps[g * 4] for g in range(31)]
+    assert spacing[0] == spacing[1]
+    for g in range(2, 31):
+        assert spacing[g] == 2 * spacing[g - 1], g
+
+
+def pin_e5m2_encode(oracle):
+    table = torch_e5m2_table()
+    for c in range(256):
+        if np.isfinite(table[c]):
+            assert oracle.e5m2_encode(table[c]) == c, hex(c)
+    pos = table[:0x7C].astype(np.float64)
+    for c in range(0x7A):
+        mid = (pos[c] + pos[c + 1]) / 2
+        assert float(np.float32(mid)) == mid
+        even = c if c % 2 == 0 else c + 1
+        for sgn, mask in ((1.0, 0x00), (-1.0, 0x80)):
+            m = np.float32(sgn * mid)
+            assert oracle.e5m2_encode(m) == (even | mask), (c, sgn)
+            assert oracle.e5m2_encode(nextafter32(m, sgn * np.inf)) == ((c + 1) | mask)
+            assert oracle.e5m2_encode(nextafter32(m, 0.0)) == (c | mask)
+    g = np.random.default_rng(4321)
+    mag = np.exp2(g.uniform(-20, math.log2(57344), 20000)).astype(np.float32)
+    y = np.concatenate([mag, -mag])
+    y = y[np.abs(y) <= 57344]
+    assert np.array_equal(oracle.e5m2_encode_array(y), torch_e5m2_encode(y))
+    for v in (57344.0, 57345.0, 61439.0, 61440.0, 1e30, math.inf):
+        assert oracle.e5m2_encode(v) == 0x7B and oracle.e5m2_encode(-v) == 0xFB, v
+    assert oracle.e5m2_encode(math.nan) == 0x7F
+    for v, code in ((2.0 ** -17, 0x00), (float(nextafter32(2.0 ** -17, 1)), 0x01),
+                    (3 * 2.0 ** -17, 0x02), (-0.0, 0x80), (-1e-30, 0x80)):
+        assert oracle.e5m2_encode(v) == code, v
+
+
+def pin_variant_scale_and_tail(oracle):
+    g = np.random.default_rng(17)
+    for fmt in (E4M3, E5M2):
+        for a in np.exp2(g.uniform(-60, 60, 300)).astype(np.float32):
+            s, inv = oracle.block_scale_fmt(a, fmt)
+            assert s == a / np.float32(FP8_MAX[fmt])
+            assert inv == np.float32(FP8_MAX[fmt]) / a
+        for block in VARIANT_BLOCKS:
+            n = 3 * block + block // 2 + 3
+            x = g.standard_normal(n).astype(np.float32)
+            codes, scales = oracle.quantize_fmt(x, block, fmt)
+            assert scales.size == -(-n // block)
+            for b in range(scales.size):
+                blk = x[b * block:(b + 1) * block]
+                assert scales[b] == np.float32(np.max(np.abs(blk))) / np.float32(FP8_MAX[fmt])
+                one_c, one_s = oracle.quantize_fmt(blk, block, fmt)
+                assert np.array_equal(codes[b * block:(b + 1) * block], one_c)
+    # the E4M3 / 128 variant is the main path
+    x = W.random_inputs(1, 1000, BF16, 3, scale_spread=2.0)[0]
+    c1, s1 = oracle.quantize(x)
+    c2, s2 = oracle.quantize_fmt(x, 128, E4M3)
+    assert np.array_equal(c1, c2) and same_bits(s1, s2)
+
+
+def pin_variant_roundtrip_and_bound(oracle):
+    g = np.random.default_rng(23)
+    tables = {E4M3: torch_e4m3_table(), E5M2: torch_e5m2_table()}
+    for fmt in (E4M3, E5M2):
+        table = tables[fmt]
+        finite = np.array([c for c in range(256) if np.isfinite(table[c])], dtype=np.uint8)
+        top = 0x7E if fmt == E4M3 else 0x7B
+        for block in VARIANT_BLOCKS:
+            for j in (-12, 0, 9):
+                codes = g.choice(finite, size=block * 3)
+                codes[::block] = top
+                x = (table[codes] * np.float32(2.0 ** j)).astype(np.float32)
+                qc, qs = oracle.quantize_fmt(x, block, fmt)
+                assert np.array_equal(qc, codes) and np.all(qs == np.float32(2.0 ** j))
+                assert same_bits(oracle.dequantize_fmt(qc, qs, block, fmt), x)
+            # error bound: 2^-(m+1) relative for normals (m mantissa bits),
+            # half a subnormal step times s below the normal range
+            x = W.random_inputs(1, block * 20 + 7, F32, block + fmt, scale_spread=4.0)[0]
+            qc, qs = oracle.quantize_fmt(x, block, fmt)
+            back = oracle.dequantize_fmt(qc, qs, block, fmt).astype(np.float64)
+            s = np.repeat(qs.astype(np.float64), block)[:x.size]
+            x64 = x.astype(np.float64)
+            y = np.where(s > 0, np.abs(x64) / np.where(s > 0, s, 1), 0)
+            rel = 2.0 ** -4 if fmt == E4M3 else 2.0 ** -3
+            min_normal = 2.0 ** -6 if fmt == E4M3 else 2.0 ** -14
+            half_sub = 2.0 ** -10 if fmt == E4M3 else 2.0 ** -17
+            err = np.abs(back - x64)
+            normal = y >= min_normal
+            assert np.all(err[normal] <= rel * np.abs(x64[normal]))
+            assert np.all(err[~normal] <= half_sub * s[~normal] * (1 + 2.0 ** -20) +
+                          2.0 ** -22 * np.abs(x64[~normal]))
+
+
+def pin_variant_reduce(oracle):
+    for fmt in (E4M3, E5M2):
+        for block in VARIANT_BLOCKS:
+            ins = W.random_inputs(4, block * 6 + 5, F32, 40 + block + fmt, scale_spread=3.0)
+            pays = [oracle.quantize_fmt(x, block, fmt) for x in ins]
+            out = oracle.reduce_fmt([c for c, _ in pays], [s for _, s in pays], block, fmt)
+            T = np.sum([x.astype(np.float64) for x in ins], axis=0)
+            # each dequantized value sums exactly as the dequantized payloads
+            v = [oracle.dequantize_fmt(c, s, block, fmt).astype(np.float64) for c, s in pays]
+            rel = 2.0 ** -4 if fmt == E4M3 else 2.0 ** -3
+            half_sub = 2.0 ** -10 if fmt == E4M3 else 2.0 ** -17
+            bound = np.zeros(T.size)
+            for x, (c, s) in zip(ins, pays):
+                bound += rel * np.abs(x) + half_sub * np.repeat(s.astype(np.float64),
+                                                                block)[:x.size] * 1.000001
+            bound += 3 * 2.0 ** -24 * np.sum(np.abs(v), axis=0) * 1.0001 + 1e-45
+            assert np.all(np.abs(out.astype(np.float64) - T) <= bound), (fmt, block)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -19,7 +19,8 @@ MUTANTS = [
     ("sub_ties_away", "m = nearbyint(a * 0x1p9);", "m = round(a * 0x1p9);"),
     ("sat_to_nan", "return sign | 0x7E;", "return 0x7F;"),
     ("sub_scale", "m = nearbyint(a * 0x1p9);", "m = nearbyint(a * 0x1p8);"),
-    ("max_240", "float q = 448.0f / amax;", "float q = 240.0f / amax;"),
+    ("max_240", "return fmt == ORC_E5M2 ? 57344.0f : 448.0f;",
+     "return fmt == ORC_E5M2 ? 57344.0f : 240.0f;"),
     ("divide_not_reciprocal", "float y = v[i] * inv;", "float y = v[i] / s;"),
     ("degenerate_sign", "codes[i] = signbit(v[i]) ? 0x80 : 0x00;", "codes[i] = 0x00;"),
     ("no_fabs", "amax = fmaxf(amax, fabsf(v[i]));", "amax = fmaxf(amax, v[i]);"),
@@ -39,12 +40,14 @@ MUTANTS = [
      "                       dequant_elem(shard_codes, shard_scales, block, i));",
      "                       reduced[i]);"),
     ("tail_block_dropped",
-     "    nb = (n + (size_t)block - 1) / (size_t)block;\n    for (b = 0; b < nb; b++) {",
-     "    nb = n / (size_t)block;\n    for (b = 0; b < nb; b++) {"),
+     "    float buf[128];\n    size_t b, nb, lo, len, i;\n    if (check_dtype(dtype) || check_block(block))\n        return check_dtype(dtype) ? ORC_ERR_ARG : ORC_ERR_UNSUPPORTED;\n    nb = (n + (size_t)block - 1) / (size_t)block;",
+     "    float buf[128];\n    size_t b, nb, lo, len, i;\n    if (check_dtype(dtype) || check_block(block))\n        return check_dtype(dtype) ? ORC_ERR_ARG : ORC_ERR_UNSUPPORTED;\n    nb = n / (size_t)block;"),
     ("shard_len_unrounded",
      "        per = (per + (size_t)block - 1) / (size_t)block * (size_t)block;",
      "        per = per;"),
-    ("subnormal_sign_lost", "        return sign | (uint8_t)m;", "        return (uint8_t)m;"),
+    ("subnormal_sign_lost",
+     "         * code (exponent 1, mantissa 0) is also 8. */\n        m = nearbyint(a * 0x1p9);\n        return sign | (uint8_t)m;",
+     "         * code (exponent 1, mantissa 0) is also 8. */\n        m = nearbyint(a * 0x1p9);\n        return (uint8_t)m;"),
     ("rs_wrong_offset", "            store_elem(out[owner], dtype, i - lo, sum);",
      "            store_elem(out[owner], dtype, i - lo + (owner > 0), sum);"),
     ("ag_own_contribution",
@@ -53,6 +56,15 @@ MUTANTS = [
     ("a2a_transposed",
      "                store_elem(out[j], dtype, (size_t)r * c + i, v);",
      "                store_elem(out[r], dtype, (size_t)j * c + i, v);"),
+    ("e5m2_bias", "ldexp((double)(4 + m), e - 17)", "ldexp((double)(4 + m), e - 16)"),
+    ("e5m2_max", "return fmt == ORC_E5M2 ? 57344.0f : 448.0f;",
+     "return fmt == ORC_E5M2 ? 49152.0f : 448.0f;"),
+    ("e5m2_ties_away", "m = nearbyint(ldexp(a, 2 - e));", "m = round(ldexp(a, 2 - e));"),
+    ("e5m2_inf_as_nan", "        return m ? NAN : (sign ? -INFINITY : INFINITY);",
+     "        return NAN;"),
+    ("e5m2_saturates_to_inf", "        return sign | 0x7B;", "        return sign | 0x7C;"),
+    ("variant_block_fixed", "        len = (n - lo < (size_t)block) ? n - lo : (size_t)block;\n        for (i = 0; i < len; i++)\n            buf[i] = load_elem(in, dtype, lo + i);\n        scales[b] = quantize_block_fmt(buf, len, codes + lo, fmt);",
+     "        len = (n - lo < (size_t)block) ? n - lo : (size_t)block;\n        for (i = 0; i < len; i++)\n            buf[i] = load_elem(in, dtype, lo + i);\n        scales[b] = quantize_block_fmt(buf, len, codes + lo, block == 256 ? 0 : fmt);"),
     ("a2a_global_blocks",
      "                st = orc_quantize(elem_ptr(in[r], dtype, (size_t)j * c), dtype, c, block,\n                                  wire_codes[r] + (size_t)j * c,\n                                  wire_scales[r] + (size_t)j * nbc);",
      "                st = j ? 0 : orc_quantize(in[r], dtype, c * (size_t)nranks, block,\n                                          wire_codes[r], wire_scales[r]);"),
