@@ -433,6 +433,58 @@ def measure_collectives(torch, stream, iters=20):
     return out
 
 
+def measure_variants(torch, stream, n=1 << 22, iters=10):
+    """Ablation of the FP8 format and block size (staged path: quantize each
+    of 8 ranks, then reduce), on the gradient workload's recipe at n elements
+    per rank: error of the FP32 result against the FP64 sum of the inputs,
+    compression ratio, and time per allreduce (L2 flushed)."""
+    import precision_collective_reduction_gb300 as pcr
+    w = W.LP_GRAD_N8_256MB_F32
+    N = w.nranks
+    ins = [torch.from_numpy(x).cuda() for x in W.draw_all(w, n)]
+    exact = torch.zeros(n, dtype=torch.float64, device="cuda")
+    for t in ins:
+        exact += t.double()
+    norm = float(torch.linalg.vector_norm(exact))
+    peak = float(exact.abs().max())
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    codes = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(N)]
+    scales = [torch.empty(pcr.nblocks(n, 32), dtype=torch.float32, device="cuda")
+              for _ in range(N)]
+    scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    res = {"workload": "%s recipe, %d elements per rank, FP32" % (w.name, n)}
+    for fmt, fname in ((pcr.E4M3, "E4M3"), (pcr.E5M2, "E5M2")):
+        for block in pcr.VARIANT_BLOCKS:
+            def step():
+                for r in range(N):
+                    pcr.lp_quantize_fmt(ins[r], codes[r], scales[r], block, fmt,
+                                        stream=stream)
+                pcr.lp_reduce_fmt(codes, scales, out, block, fmt, stream=stream)
+            with torch.cuda.stream(stream):
+                step()
+            torch.cuda.synchronize()
+            err = out.double() - exact
+            times = []
+            with torch.cuda.stream(stream):
+                for _ in range(iters):
+                    flush_l2(torch, scratch)
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    step()
+                    b.record(stream)
+                    b.synchronize()
+                    times.append(a.elapsed_time(b) * 1e3)
+            res["%s/%d" % (fname, block)] = {
+                "rel_l2_error": float(torch.linalg.vector_norm(err)) / norm,
+                "max_abs_error_over_max": float(err.abs().max()) / peak,
+                "compression": round(4 / (1 + 4 / block), 4),
+                "us_staged": round(statistics.median(times), 2)}
+    del ins, exact, out, codes, scales, scratch
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -512,6 +564,7 @@ def run_ours(args):
             for wl in (W.LP_FLAT_N2_1M_F32, W.LP_FLAT_N8_16MB_BF16,
                        W.LP_TREE_N8_64MB_BF16)}
         extras["collectives_lp_n8_16MiB_bf16"] = measure_collectives(torch, stream)
+        extras["ablation_fp8_block"] = measure_variants(torch, stream)
     clocks.stop()
 
     if rank != 0:

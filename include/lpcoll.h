@@ -60,6 +60,9 @@ extern "C" {
 
 typedef enum { LPCOLL_F32 = 0, LPCOLL_BF16 = 1 } lpcoll_dtype;
 
+/* FP8 formats of the *_fmt variants (the main path is E4M3). */
+typedef enum { LPCOLL_E4M3 = 0, LPCOLL_E5M2 = 1 } lpcoll_fp8;
+
 typedef enum {
     LPCOLL_OK = 0,
     LPCOLL_ERR_ARG = 1,         /* bad dtype, nranks, or a NULL pointer */
@@ -132,6 +135,25 @@ int dda_tree_sim(const void *const *in, void *const *out, int nranks,
                  size_t n, lpcoll_dtype dtype, int block,
                  uint8_t *const *wire_codes, float *const *wire_scales,
                  uint8_t *shard_codes, float *shard_scales, void *stream);
+
+/* Format and block-size variants of lp_quantize / lp_dequantize / lp_reduce,
+ * for ablations (the pages fix neither; the main path is E4M3 with blocks of
+ * 128). fmt: LPCOLL_E4M3 (largest finite 448) or LPCOLL_E5M2 (largest
+ * finite 57344, Inf/NaN codes never produced: values saturate). block: 32,
+ * 64, 128 or 256 elements per FP32 scale (else LPCOLL_ERR_UNSUPPORTED); a
+ * payload of n elements is codes[n] plus scales[ceil(n/block)], block b
+ * covering elements [b block, (b+1) block). Scale s = a / max, codes =
+ * fp8(x * (max / a)), rounded to nearest even and saturated; values are
+ * fl(fp8 * s), reduced in FP32 in rank order. With LPCOLL_E4M3 and block 128
+ * they return exactly what the plain entry points return.                 */
+int lp_quantize_fmt(const void *in, lpcoll_dtype dtype, size_t n, int block,
+                    lpcoll_fp8 fmt, uint8_t *codes, float *scales, void *stream);
+int lp_dequantize_fmt(const uint8_t *codes, const float *scales, size_t n,
+                      int block, lpcoll_fp8 fmt, void *out, lpcoll_dtype dtype,
+                      void *stream);
+int lp_reduce_fmt(const uint8_t *const *codes, const float *const *scales,
+                  int nranks, size_t n, int block, lpcoll_fp8 fmt, void *out,
+                  lpcoll_dtype dtype, void *stream);
 
 /* ReduceScatter over nranks emulated ranks: rank r receives shard r of the
  * sum of all ranks' messages. Pages: "Funcionalidade Principal 2", feature

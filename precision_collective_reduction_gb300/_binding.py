@@ -17,6 +17,9 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "lpcoll.h")
 F32 = 0
 BF16 = 1
 BLOCK = 128
+E4M3 = 0
+E5M2 = 1
+VARIANT_BLOCKS = (32, 64, 128, 256)
 MAX_RANKS = 16
 
 STATUS = {0: "LPCOLL_OK", 1: "LPCOLL_ERR_ARG", 2: "LPCOLL_ERR_ALIGN",
@@ -50,9 +53,13 @@ def lib():
         for f in ("reduce_scatter_sim", "all_gather_sim", "all_to_all_sim"):
             getattr(L, f).argtypes = [pp, pp, ci, sz, ci, ci, pp, pp, vp]
         L.dda_flat_sim_noalloc.argtypes = [pp, pp, ci, sz, ci, vp]
+        L.lp_quantize_fmt.argtypes = [vp, ci, sz, ci, ci, vp, vp, vp]
+        L.lp_dequantize_fmt.argtypes = [vp, vp, sz, ci, ci, vp, ci, vp]
+        L.lp_reduce_fmt.argtypes = [pp, pp, ci, sz, ci, ci, vp, ci, vp]
         for f in ("lp_quantize", "lp_dequantize", "lp_reduce", "dda_flat_sim",
                   "dda_tree_sim", "reduce_scatter_sim", "all_gather_sim",
-                  "all_to_all_sim", "dda_flat_sim_noalloc",
+                  "all_to_all_sim", "dda_flat_sim_noalloc", "lp_quantize_fmt",
+                  "lp_dequantize_fmt", "lp_reduce_fmt",
                   "lpcoll_last_cuda_error", "lpcoll_version"):
             getattr(L, f).restype = ci
         L.lpcoll_status_string.argtypes = [ci]
@@ -334,3 +341,41 @@ def dda_flat_sim_noalloc(ins, outs, stream=None):
     op = [_need(t, "out[%d]" % r, dt, n) for r, t in enumerate(outs)]
     raw_dda_flat_sim_noalloc(ip, op, len(ip), n, dtype_code(ins[0]), _stream(stream))
     return outs
+
+
+def lp_quantize_fmt(x, codes, scales, block, fmt, stream=None):
+    """Format / block-size variant of lp_quantize (fmt E4M3 or E5M2; block 32,
+    64, 128 or 256)."""
+    torch = _torch()
+    n = x.numel()
+    xp = _need(x, "x")
+    cp = _need(codes, "codes", torch.uint8, n)
+    sp = _need(scales, "scales", torch.float32, nblocks(n, block))
+    _check(lib().lp_quantize_fmt(xp, dtype_code(x), n, block, fmt, cp, sp,
+                                 _stream(stream)), "lp_quantize_fmt")
+    return codes, scales
+
+
+def lp_dequantize_fmt(codes, scales, out, block, fmt, stream=None):
+    torch = _torch()
+    n = out.numel()
+    op = _need(out, "out")
+    cp = _need(codes, "codes", torch.uint8, n)
+    sp = _need(scales, "scales", torch.float32, nblocks(n, block))
+    _check(lib().lp_dequantize_fmt(cp, sp, n, block, fmt, op, dtype_code(out),
+                                   _stream(stream)), "lp_dequantize_fmt")
+    return out
+
+
+def lp_reduce_fmt(codes, scales, out, block, fmt, stream=None):
+    torch = _torch()
+    n = out.numel()
+    op = _need(out, "out")
+    cps = [_need(c, "codes[%d]" % r, torch.uint8, n) for r, c in enumerate(codes)]
+    sps = [_need(s, "scales[%d]" % r, torch.float32, nblocks(n, block))
+           for r, s in enumerate(scales)]
+    if len(cps) != len(sps):
+        raise ValueError("codes and scales must list the same ranks")
+    _check(lib().lp_reduce_fmt(ptr_array(cps), ptr_array(sps), len(cps), n, block, fmt,
+                               op, dtype_code(out), _stream(stream)), "lp_reduce_fmt")
+    return out

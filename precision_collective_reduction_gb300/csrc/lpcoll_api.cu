@@ -22,6 +22,13 @@ cudaError_t launch_reduce(const ReduceParams &p, int nranks, size_t n, void *out
                           int dtype, cudaStream_t stream);
 cudaError_t launch_all_gather(const DdaParams &p, int nranks, size_t m, int dtype,
                               bool lp, cudaStream_t st);
+cudaError_t launch_quantize_fmt(const void *in, int dtype, size_t n, int block, int fmt,
+                                uint8_t *codes, float *scales, cudaStream_t st);
+cudaError_t launch_dequantize_fmt(const uint8_t *codes, const float *scales, size_t n,
+                                  int block, int fmt, void *out, int dtype,
+                                  cudaStream_t st);
+cudaError_t launch_reduce_fmt(const ReduceParams &p, int nranks, size_t n, int block,
+                              int fmt, void *out, int dtype, cudaStream_t st);
 cudaError_t launch_all_to_all(const DdaParams &p, int nranks, size_t c, int dtype,
                               bool lp, cudaStream_t st);
 
@@ -188,6 +195,16 @@ int collective_args(const void *const *in, void *const *out, int nranks, int dty
     return LPCOLL_OK;
 }
 
+// dtype / format / block of the *_fmt variants.
+int check_variant(int dtype, int fmt, int block)
+{
+    if (bad_dtype(dtype) || (fmt != LPCOLL_E4M3 && fmt != LPCOLL_E5M2))
+        return LPCOLL_ERR_ARG;
+    if (block != 32 && block != 64 && block != 128 && block != 256)
+        return LPCOLL_ERR_UNSUPPORTED;
+    return LPCOLL_OK;
+}
+
 int check_common(int dtype, int nranks, int block)
 {
     if (bad_dtype(dtype) || nranks < 1 || nranks > LPCOLL_MAX_RANKS)
@@ -334,6 +351,54 @@ int all_to_all_sim(const void *const *in, void *const *out, int nranks, size_t c
     if (st != LPCOLL_OK)
         return st;
     return finish(launch_all_to_all(p, nranks, c, dtype, block != 0,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+int lp_quantize_fmt(const void *in, lpcoll_dtype dtype, size_t n, int block,
+                    lpcoll_fp8 fmt, uint8_t *codes, float *scales, void *stream)
+{
+    int st = check_variant(dtype, fmt, block);
+    if (st != LPCOLL_OK || n == 0)
+        return st;
+    st = first_error({check_ptr(in), check_ptr(codes), check_ptr(scales)});
+    if (st != LPCOLL_OK)
+        return st;
+    return finish(launch_quantize_fmt(in, dtype, n, block, fmt, codes, scales,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int lp_dequantize_fmt(const uint8_t *codes, const float *scales, size_t n, int block,
+                      lpcoll_fp8 fmt, void *out, lpcoll_dtype dtype, void *stream)
+{
+    int st = check_variant(dtype, fmt, block);
+    if (st != LPCOLL_OK || n == 0)
+        return st;
+    st = first_error({check_ptr(codes), check_ptr(scales), check_ptr(out)});
+    if (st != LPCOLL_OK)
+        return st;
+    return finish(launch_dequantize_fmt(codes, scales, n, block, fmt, out, dtype,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int lp_reduce_fmt(const uint8_t *const *codes, const float *const *scales, int nranks,
+                  size_t n, int block, lpcoll_fp8 fmt, void *out, lpcoll_dtype dtype,
+                  void *stream)
+{
+    int st = check_variant(dtype, fmt, block);
+    if (st == LPCOLL_OK && (nranks < 1 || nranks > LPCOLL_MAX_RANKS))
+        st = LPCOLL_ERR_ARG;
+    if (st != LPCOLL_OK || n == 0)
+        return st;
+    st = first_error({check_rank_array(codes, nranks), check_rank_array(scales, nranks),
+                      check_ptr(out)});
+    if (st != LPCOLL_OK)
+        return st;
+    ReduceParams p = {};
+    for (int r = 0; r < nranks; ++r) {
+        p.codes[r] = codes[r];
+        p.scales[r] = scales[r];
+    }
+    return finish(launch_reduce_fmt(p, nranks, n, block, fmt, out, dtype,
                                     static_cast<cudaStream_t>(stream)));
 }
 

@@ -157,3 +157,21 @@ def test_collective_validation(L, fn):
                  None) == ARG                                       # wires first
     else:
         assert f(two, arr(A, None), 2, 10, 0, 0, None, None, None) == RANK
+
+
+def test_variant_validation(L):
+    two = arr(A, A)
+    assert L.lp_quantize_fmt(A, 0, 10, 128, 2, A, A, None) == ARG       # format
+    assert L.lp_quantize_fmt(A, 2, 10, 128, 0, A, A, None) == ARG       # dtype
+    for bad in (0, 16, 48, 512):
+        assert L.lp_quantize_fmt(A, 0, 10, bad, 1, A, A, None) == UNSUP
+    assert L.lp_quantize_fmt(None, 0, 0, 64, 1, None, None, None) == OK
+    assert L.lp_quantize_fmt(A, 1, 10, 32, 1, None, A, None) == ARG
+    assert L.lp_quantize_fmt(A, 1, 10, 256, 0, A, A + 4, None) == ALIGN
+    assert L.lp_dequantize_fmt(A, A, 10, 64, 3, A, 0, None) == ARG
+    assert L.lp_dequantize_fmt(A, A, 10, 100, 0, A, 0, None) == UNSUP
+    assert L.lp_dequantize_fmt(A, A, 10, 64, 1, A + 2, 1, None) == ALIGN
+    assert L.lp_reduce_fmt(two, two, 0, 10, 64, 1, A, 0, None) == ARG
+    assert L.lp_reduce_fmt(two, two, 2, 10, 96, 1, A, 0, None) == UNSUP
+    assert L.lp_reduce_fmt(arr(A, None), two, 2, 10, 64, 1, A, 0, None) == RANK
+    assert L.lp_reduce_fmt(two, two, 2, 10, 64, 1, None, 0, None) == ARG
