@@ -8,6 +8,7 @@
 #include <initializer_list>
 #include <mutex>
 #include <unordered_map>
+#include <utility>
 
 #include "lpcoll.h"
 #include "lpcoll_dda.cuh"
@@ -49,27 +50,31 @@ struct OccHash {
 };
 
 std::mutex g_occ_mutex;
-std::unordered_map<OccKey, int, OccHash> g_wave;  // CTAs of one launch wave
+// SM count and resident CTAs per SM of each kernel on each device
+std::unordered_map<OccKey, std::pair<int, int>, OccHash> g_wave;
 
-int full_wave(const void *kernel)
+int full_wave(const void *kernel, int cap)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return 1;
-    std::lock_guard<std::mutex> lock(g_occ_mutex);
-    auto it = g_wave.find(OccKey{kernel, dev});
-    if (it != g_wave.end())
-        return it->second;
     int sms = 0, per_sm = 0;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
-    if (per_sm > kCtasPerSm)
-        per_sm = kCtasPerSm;
-    int wave = sms * per_sm;
-    if (wave < 1)
-        wave = 1;
-    g_wave.emplace(OccKey{kernel, dev}, wave);
-    return wave;
+    {
+        std::lock_guard<std::mutex> lock(g_occ_mutex);
+        auto it = g_wave.find(OccKey{kernel, dev});
+        if (it != g_wave.end()) {
+            sms = it->second.first;
+            per_sm = it->second.second;
+        } else {
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+            g_wave.emplace(OccKey{kernel, dev}, std::make_pair(sms, per_sm));
+        }
+    }
+    if (per_sm > cap)
+        per_sm = cap;
+    const int wave = sms * per_sm;
+    return wave < 1 ? 1 : wave;
 }
 
 inline bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
@@ -216,10 +221,10 @@ int check_common(int dtype, int nranks, int block)
 
 }  // namespace
 
-int wave_ctas(const void *kernel, size_t units)
+int wave_ctas(const void *kernel, size_t units, int cap)
 {
     const size_t need = (units + kWarpsPerCta - 1) / kWarpsPerCta;
-    const size_t wave = static_cast<size_t>(full_wave(kernel));
+    const size_t wave = static_cast<size_t>(full_wave(kernel, cap));
     const size_t g = need < wave ? need : wave;
     return static_cast<int>(g < 1 ? 1 : g);
 }

@@ -17,9 +17,10 @@
 // Every element is read before any output of its unit is written, so an
 // output may alias its input.
 //
-// The warps stride over units (grid-stride loop); the grid is at most
-// kCtasPerSm CTAs per SM, all resident at once, so the units of every rank
-// stream through HBM in order.
+// The warps stride over units (grid-stride loop); the grid is at most 2 CTAs
+// per SM for large allreduces and 4 otherwise (kCtasPerSm / kCtasPerSmBusy),
+// all resident at once, so the units of every rank stream through HBM in
+// order.
 #pragma once
 
 #include "lpcoll_device.cuh"
@@ -195,8 +196,8 @@ inline void unit_counts(size_t n, size_t &full, size_t &total)
 }
 
 // CTAs for a launch covering `units` warp-units: enough for every unit, at
-// most min(resident CTAs per SM, kCtasPerSm) x SMs.
-int wave_ctas(const void *kernel, size_t units);
+// most min(resident CTAs per SM, cap) x SMs.
+int wave_ctas(const void *kernel, size_t units, int cap = kCtasPerSmBusy);
 
 template <int N, int DT, int MODE>
 cudaError_t launch_dda_n(const DdaParams &p, size_t n, cudaStream_t stream)
@@ -205,7 +206,10 @@ cudaError_t launch_dda_n(const DdaParams &p, size_t n, cudaStream_t stream)
     unit_counts<DT>(n, full, total);
     const void *k = reinterpret_cast<const void *>(&dda_kernel<N, DT, MODE>);
     const size_t K = units_per_iter<N>();
-    const int grid = wave_ctas(k, (total + K - 1) / K);
+    const bool scatter = (MODE == kScatterExact || MODE == kScatterLp);
+    const size_t in_bytes = n * static_cast<size_t>(N) * (16 / Fmt<DT>::kVec);
+    const int cap = (scatter || in_bytes < kSmallLaunchBytes) ? kCtasPerSmBusy : kCtasPerSm;
+    const int grid = wave_ctas(k, (total + K - 1) / K, cap);
     dda_kernel<N, DT, MODE><<<grid, kThreads, 0, stream>>>(p, n, full, total);
     return cudaGetLastError();
 }

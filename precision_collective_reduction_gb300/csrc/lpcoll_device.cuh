@@ -27,9 +27,14 @@ constexpr int kBlock = LPCOLL_BLOCK;  // elements per scale block
 constexpr float kE4M3Max = 448.0f;    // largest finite E4M3 value
 constexpr int kThreads = 256;         // threads per CTA of every kernel
 constexpr int kWarpsPerCta = kThreads / 32;
-// Resident CTAs per SM the launches aim for (at most): 16 warps per SM keep
-// enough 16-byte loads in flight and streamed HBM faster than 32 warps.
+// Resident CTAs per SM a launch aims for (at most). Measured on GB300: large
+// allreduces (>= kSmallLaunchBytes of input) stream HBM fastest with 16
+// warps per SM (2 CTAs; 4 CTAs cost 3-4%); smaller allreduces, the
+// read-heavy reduce-scatter and the one-sender-per-warp kernels (gather,
+// all-to-all, codec) gain 4-23% from 4 CTAs.
 constexpr int kCtasPerSm = 2;
+constexpr int kCtasPerSmBusy = 4;
+constexpr size_t kSmallLaunchBytes = size_t(256) << 20;
 
 // What a fused launch computes: the allreduce (exact, LP flat, LP tree) or a
 // reduce-scatter (exact or LP), whose result goes to the shard's owner only.
