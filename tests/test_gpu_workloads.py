@@ -86,3 +86,66 @@ def test_workload(oracle, w):
             _check(pick_s(bufs.shard_scales), o_ss, "shard_scales")
     del bufs
     torch.cuda.empty_cache()
+
+
+def test_collectives_at_benchmark_size(oracle):
+    """ReduceScatter, AllGather and AlltoAll in the benchmark's configuration
+    (8 ranks, 16 MiB BF16 per rank, low precision), checked on sampled
+    128-element blocks against the oracle (blocks are independent)."""
+    import precision_collective_reduction_gb300 as pcr
+    w = W.LP_FLAT_N8_16MB_BF16
+    N, n = w.nranks, w.n
+    ins = W.draw_all(w)
+    dins = [torch.from_numpy(x).view(torch.int16).view(torch.bfloat16).cuda() for x in ins]
+    nb = pcr.nblocks(n)
+    wc = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(N)]
+    ws = [torch.empty(nb, dtype=torch.float32, device="cuda") for _ in range(N)]
+    g = np.random.default_rng(77)
+
+    # reduce-scatter: shard r of the flat allreduce, on sampled blocks
+    per = pcr.shard_len(n, N)
+    rs = [torch.empty(max(1, min(per, n - r * per)), dtype=torch.bfloat16, device="cuda")
+          for r in range(N)]
+    pcr.reduce_scatter_sim(dins, rs, wire_codes=wc, wire_scales=ws)
+    torch.cuda.synchronize()
+    blocks = sorted(set(g.choice(nb, 64, replace=False).tolist()) | {0, nb - 1})
+    sub = [_gather_blocks(x, blocks, n) for x in ins]
+    want = oracle.flat(sub)[0][0]
+    got = []
+    for b in blocks:
+        owner, off = divmod(b * 128, per)
+        got.append(from_dev(rs[owner][off:off + 128]))
+    _check(np.concatenate(got), want, "reduce_scatter sampled blocks")
+
+    # all-gather of the first m elements of every rank
+    m = n // N
+    outs = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+    pcr.all_gather_sim([t[:m] for t in dins], outs, wire_codes=wc, wire_scales=ws)
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    mb = m // 128
+    for r in range(N):
+        for b in g.choice(mb, 8, replace=False).tolist() + [mb - 1]:
+            blk = ins[r][b * 128:(b + 1) * 128]
+            c, s = oracle.quantize(blk)
+            want = oracle.dequantize(c, s, dtype=np.uint16)
+            at = r * m + b * 128
+            _check(from_dev(outs[-1][at:at + 128]), want, "all_gather r=%d b=%d" % (r, b))
+
+    # all-to-all with chunks of c = n / N
+    c = n // N
+    pcr.all_to_all_sim(dins, outs, wire_codes=wc, wire_scales=ws)
+    torch.cuda.synchronize()
+    cb = c // 128
+    for r in range(N):
+        for j in range(N):
+            for b in g.choice(cb, 3, replace=False).tolist() + [cb - 1]:
+                blk = ins[r][j * c + b * 128:j * c + (b + 1) * 128]
+                cc, ss = oracle.quantize(blk)
+                want = oracle.dequantize(cc, ss, dtype=np.uint16)
+                at = r * c + b * 128
+                _check(from_dev(outs[j][at:at + 128]), want,
+                       "all_to_all r=%d j=%d b=%d" % (r, j, b))
+    del dins, wc, ws, rs, outs
+    torch.cuda.empty_cache()
