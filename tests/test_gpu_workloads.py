@@ -149,3 +149,36 @@ def test_collectives_at_benchmark_size(oracle):
                        "all_to_all r=%d j=%d b=%d" % (r, j, b))
     del dins, wc, ws, rs, outs
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("block", [32, 64, 128, 256])
+def test_variants_at_benchmark_size(oracle, fmt, block):
+    """The format / block-size ablation's configuration (8 ranks x 4 Mi FP32,
+    gradient recipe): quantize and reduce on the GPU, sampled blocks of the
+    payload and of the reduced result against the oracle."""
+    import precision_collective_reduction_gb300 as pcr
+    w = W.LP_GRAD_N8_256MB_F32
+    n = 1 << 22
+    ins = W.draw_all(w, n)
+    dins = [torch.from_numpy(x).cuda() for x in ins]
+    codes = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(w.nranks)]
+    scales = [torch.empty(pcr.nblocks(n, block), dtype=torch.float32, device="cuda")
+              for _ in range(w.nranks)]
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    for r in range(w.nranks):
+        pcr.lp_quantize_fmt(dins[r], codes[r], scales[r], block, fmt)
+    pcr.lp_reduce_fmt(codes, scales, out, block, fmt)
+    torch.cuda.synchronize()
+    nb = n // block
+    g = np.random.default_rng(block + fmt)
+    for b in g.choice(nb, 32, replace=False).tolist() + [0, nb - 1]:
+        lo, hi = b * block, (b + 1) * block
+        pays = [oracle.quantize_fmt(x[lo:hi], block, fmt) for x in ins]
+        for r in (0, w.nranks - 1):
+            _check(from_dev(codes[r][lo:hi]), pays[r][0], "codes r=%d b=%d" % (r, b))
+            _check(from_dev(scales[r][b:b + 1]), pays[r][1], "scale r=%d b=%d" % (r, b))
+        want = oracle.reduce_fmt([c for c, _ in pays], [s for _, s in pays], block, fmt)
+        _check(from_dev(out[lo:hi]), want, "reduced b=%d" % b)
+    del dins, codes, scales, out
+    torch.cuda.empty_cache()
