@@ -629,6 +629,27 @@ def run_crossover(args):
     return 0
 
 
+def _collective_runner(torch, bufs, kind):
+    """run(algo, stream) for a reduce-scatter ("rs"), all-gather of the first
+    n/N elements of every rank ("ag") or all-to-all with chunks of n/N ("a2a")
+    over the buffers of a RankBuffers (low precision, its wires)."""
+    import precision_collective_reduction_gb300 as pcr
+    N, n = bufs.nranks, bufs.n
+    if kind == "rs":
+        per = pcr.shard_len(n, N)
+        outs = [torch.empty(max(1, min(per, n - r * per)), dtype=bufs.ins[0].dtype,
+                            device="cuda") for r in range(N)]
+        return lambda a, s: pcr.reduce_scatter_sim(bufs.ins, outs, wire_codes=bufs.wire_codes,
+                                                   wire_scales=bufs.wire_scales, stream=s)
+    if kind == "ag":
+        m = n // N
+        return lambda a, s: pcr.all_gather_sim([t[:m] for t in bufs.ins], bufs.outs,
+                                               wire_codes=bufs.wire_codes,
+                                               wire_scales=bufs.wire_scales, stream=s)
+    return lambda a, s: pcr.all_to_all_sim(bufs.ins, bufs.outs, wire_codes=bufs.wire_codes,
+                                           wire_scales=bufs.wire_scales, stream=s)
+
+
 def run_profile_case(args):
     """A few launches of one workload's kernels, for ncu captures: `warmup`
     untimed launches of each algorithm, then `steps` more."""
@@ -642,12 +663,15 @@ def run_profile_case(args):
     bufs = runner.RankBuffers(w.nranks, n, w.dtype, w.block, separate_tree_out=True)
     bufs.load(W.draw_all(w, n))
     s = torch.cuda.current_stream().cuda_stream
+    run = bufs.run
+    if algos[0] in ("rs", "ag", "a2a"):
+        run = _collective_runner(torch, bufs, algos[0])
     for _ in range(args.warmup):
         for a in algos:
-            bufs.run(a, s)
+            run(a, s)
     for _ in range(args.steps):
         for a in algos:
-            bufs.run(a, s)
+            run(a, s)
     torch.cuda.synchronize()
     print("profile case %s n=%d algos=%s: %d launches" % (
         w.name, n, ",".join(algos), (args.warmup + args.steps) * len(algos)))
@@ -667,7 +691,9 @@ def main():
                     help="only run a few launches of this workload (for ncu)")
     ap.add_argument("--elems", type=int, default=0,
                     help="with --profile-case: elements per rank (default: full)")
-    ap.add_argument("--algo", choices=["flat", "tree"], default=None)
+    ap.add_argument("--algo", choices=["flat", "tree", "rs", "ag", "a2a"], default=None,
+                    help="with --profile-case: the operation to run (rs, ag and a2a "
+                         "need a low-precision workload)")
     ap.add_argument("--crossover", action="store_true",
                     help="only time flat vs tree over message sizes")
     args = ap.parse_args()
