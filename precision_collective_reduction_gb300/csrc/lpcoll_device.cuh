@@ -72,9 +72,15 @@ struct ReduceParams {
 // Memory access. Messages move with plain 16-byte loads and stores (default
 // cache policy: on GB300 it sustained 3-6% more HBM bandwidth than the
 // evict-first hints at two CTAs per SM); the small code and scale stores are
-// marked evict-first. A lane holding fewer than kVec valid elements (only in
-// the last, ragged unit) falls back to element accesses; missing elements
-// read as +0, which leaves a block maximum unchanged.
+// marked evict-first.
+//
+// The count argument `cnt` of load_vec / store_vec / store_codes:
+//   cnt == kVec   a full lane at a 16-byte aligned address: one vector access;
+//   0 < cnt < kVec  the lane holding the end of the data (the ragged unit):
+//                 cnt element accesses; missing elements read as +0, which
+//                 leaves a block maximum unchanged;
+//   cnt < 0       -cnt elements at an address that may not be aligned for a
+//                 vector access (see access_count): element accesses.
 // ---------------------------------------------------------------------------
 
 template <int DT>
@@ -85,7 +91,7 @@ __device__ __forceinline__ uint4 load_vec(const void *base, size_t e0, int cnt)
     const char *p = static_cast<const char *>(base) + e0 * ES;
     if (cnt == V)
         return *reinterpret_cast<const uint4 *>(p);
-    if (cnt < 0)  // a full lane at an address that is not 16-byte aligned
+    if (cnt < 0)
         cnt = -cnt;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     uint32_t w[4] = {0u, 0u, 0u, 0u};
@@ -115,7 +121,7 @@ __device__ __forceinline__ void store_vec(void *base, size_t e0, int cnt, uint4 
         *reinterpret_cast<uint4 *>(p) = v;
         return;
     }
-    if (cnt < 0)  // a full lane at an address that is not 16-byte aligned
+    if (cnt < 0)
         cnt = -cnt;
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     if (DT == LPCOLL_F32) {
@@ -129,20 +135,12 @@ __device__ __forceinline__ void store_vec(void *base, size_t e0, int cnt, uint4 
     }
 }
 
-// As load_vec / store_vec for element offsets that may not be 16-byte
-// aligned: vector access only when `aligned` (uniform per launch) holds.
+// Count argument for an access of cnt valid elements at an offset that is
+// vector-aligned only if `aligned` (uniform per launch) holds.
 template <int DT>
-__device__ __forceinline__ uint4 load_any(const void *base, size_t e0, int cnt,
-                                          bool aligned)
+__device__ __forceinline__ int access_count(int cnt, bool aligned)
 {
-    return load_vec<DT>(base, e0, aligned ? cnt : (cnt == Fmt<DT>::kVec ? -cnt : cnt));
-}
-
-template <int DT>
-__device__ __forceinline__ void store_any(void *base, size_t e0, int cnt, uint4 v,
-                                          bool aligned)
-{
-    store_vec<DT>(base, e0, aligned ? cnt : (cnt == Fmt<DT>::kVec ? -cnt : cnt), v);
+    return (aligned || cnt != Fmt<DT>::kVec) ? cnt : -cnt;
 }
 
 // kVec codes of one lane, packed little-endian (element e0 in the low byte).

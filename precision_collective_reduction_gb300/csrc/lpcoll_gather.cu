@@ -18,14 +18,6 @@
 
 namespace lpc {
 
-// lane count argument for load_vec / store_vec / store_codes: a negative
-// count asks for element-wise access of a full lane at an unaligned offset
-template <int DT>
-__device__ __forceinline__ int access_count(int cnt, bool aligned)
-{
-    return (aligned || cnt != Fmt<DT>::kVec) ? cnt : -cnt;
-}
-
 // Units per work item: a warp loads kItemUnits consecutive units of one
 // sender before processing them, so each lane keeps kItemUnits 16-byte loads
 // in flight (one sender per item would leave the loop latency-bound). With
