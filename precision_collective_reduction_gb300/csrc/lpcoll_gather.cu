@@ -71,15 +71,18 @@ __device__ __forceinline__ void gather_item(const DdaParams &p, int nranks, size
     }
     float x[kItemUnits][V];
     encode_item<DT, LP>(p, r, 0, 0, e0, cnt, raw, true, lane, x);
+    // output by output: each receiver's slice of the item is written as one
+    // contiguous run (2% faster than unit by unit across all receivers)
     const size_t at = static_cast<size_t>(r) * m;
+    uint4 o[kItemUnits];
 #pragma unroll
-    for (int k = 0; k < kItemUnits; ++k) {
-        if (cnt[k] > 0) {
-            const uint4 o = narrow<DT>(x[k]);
-            const int a = access_count<DT>(cnt[k], ALIGNED);
-            for (int d = 0; d < nranks; ++d)
-                store_vec<DT>(p.out[d], at + e0[k], a, o);
-        }
+    for (int k = 0; k < kItemUnits; ++k)
+        o[k] = narrow<DT>(x[k]);
+    for (int d = 0; d < nranks; ++d) {
+#pragma unroll
+        for (int k = 0; k < kItemUnits; ++k)
+            if (cnt[k] > 0)
+                store_vec<DT>(p.out[d], at + e0[k], access_count<DT>(cnt[k], ALIGNED), o[k]);
     }
 }
 
@@ -126,8 +129,10 @@ __device__ __forceinline__ void alltoall_item(const DdaParams &p, size_t c, size
                           narrow<DT>(x[k]));
 }
 
+// At most 64 registers so that 4 CTAs fit per SM (7-9% faster than the 3
+// its unconstrained 74 registers allow).
 template <int DT, bool LP, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kCtasPerSmBusy)
 alltoall_kernel(const __grid_constant__ DdaParams p, int nranks, size_t c, size_t nbc,
                 size_t groups)
 {
