@@ -43,7 +43,7 @@ from precision_collective_reduction_gb300 import workloads as W  # noqa: E402
 
 HEADLINE = W.LP_GRAD_N8_256MB_F32
 METRIC = "LP allreduce-emulation GB/s"
-CPU_SAMPLE_ELEMS = 1 << 23      # cpu_baseline: first 8 Mi elements of each rank
+CPU_SAMPLE_ELEMS = 1 << 23      # cpu_baseline: 8 Mi elements per rank, same recipe
 REF_BUDGET_ELEMS = 1 << 25      # reference arm: elements per rank over all steps
 E2E_MAX_STEPS = 20
 E2E_CHUNK = 1 << 22
