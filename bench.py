@@ -290,23 +290,22 @@ def timed_steps(torch, bufs, w, stream, steps, warmup, dist, clocks):
 
 def e2e_steps(torch, w, steps, host_in, host_out, chunk):
     """Time `steps` end-to-end allreduces of pinned host buffers through the
-    public HostAllreduce API (transfers and kernels overlapped by chunk)."""
+    library's host-buffer entry point (lpcoll_host_allreduce, via
+    HostAllreduce): per step, the host->device copies of the inputs, both
+    allreduces and the device->host copies of both results, overlapped by
+    chunk. Each call returns once its results are in host memory; the events
+    bracket the calls on the first and last stream they use."""
     from precision_collective_reduction_gb300.host import HostAllreduce
     h = HostAllreduce(w.nranks, w.n, w.dtype, w.block, algos=w.algos, chunk=chunk)
-    cur = torch.cuda.current_stream()
-    h.start_after(cur)
     h.run(host_in, host_out)          # warm-up pass
-    h.finish_before(cur)
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    start.record(cur)
-    h.start_after(cur)
+    start.record(h.streams[0])
     for _ in range(steps):
         h.run(host_in, host_out)
-    h.finish_before(cur)
-    end.record(cur)
-    torch.cuda.synchronize()
+    end.record(h.streams[2])
+    end.synchronize()
     launches = h.kernel_launches_per_run()
     del h
     return start.elapsed_time(end), launches
@@ -548,8 +547,8 @@ def run_ours(args):
     e2e = {"value": round(whole_job_gbps(sbytes, e2e_n, world, e2e_ms), 2),
            "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": round(e2e_ms / e2e_n, 3), "steps": e2e_n,
-           "api": "HostAllreduce.run (chunks of %d elements, copies and kernels "
-                  "overlapped on three streams)" % E2E_CHUNK,
+           "api": "lpcoll_host_allreduce via HostAllreduce.run (chunks of %d "
+                  "elements, copies and kernels overlapped on three streams)" % E2E_CHUNK,
            "kernel_launches_per_step": e2e_launches,
            "transfer_GBps": round((h2d + d2h) / (e2e_ms / e2e_n / 1e3) / 1e9, 1)}
     del host_in, host_out

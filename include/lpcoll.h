@@ -208,6 +208,40 @@ int all_to_all_sim(const void *const *in, void *const *out, int nranks,
                    uint8_t *const *wire_codes, float *const *wire_scales,
                    void *stream);
 
+/* Allreduce of nranks messages that live in HOST memory, through a device
+ * workspace the caller provides: the flat and / or tree allreduce of
+ * dda_flat_sim / dda_tree_sim (same results, bit for bit), run chunk by
+ * chunk with host->device copies, kernels and device->host copies of
+ * different chunks overlapped. Pages: the allreduce of "Funcionalidade
+ * Principal 1" fed from and returned to host memory.
+ *   host_in[r]        rank r's message, n elements of dtype (host)
+ *   host_out_flat[r]  n elements (host) receiving the flat allreduce, or the
+ *                     whole array NULL to skip it
+ *   host_out_tree[r]  the same for the tree allreduce; at least one of the
+ *                     two arrays must be given
+ *   block             0 (exact) or 128 (low precision)
+ *   chunk             elements per chunk, a positive multiple of 128
+ *   slots             chunks in flight, 1..8 (2 or more to overlap)
+ *   workspace         device memory of workspace_bytes >=
+ *                     lpcoll_host_workspace_bytes(...), 256-byte aligned;
+ *                     its contents are scratch
+ *   copy_in_stream, compute_stream, copy_out_stream   cudaStream_t as void*
+ *                     (three distinct streams overlap; NULL serializes)
+ * Host buffers should be pinned (page-locked) for the copies to overlap.
+ * The call returns when every result is in host memory (it synchronizes
+ * copy_out_stream). Errors: LPCOLL_ERR_ARG (dtype, nranks, slots, chunk,
+ * workspace NULL or too small, no output), LPCOLL_ERR_UNSUPPORTED (block),
+ * LPCOLL_ERR_RANK (NULL per-rank pointer), LPCOLL_ERR_ALIGN (workspace),
+ * LPCOLL_ERR_CUDA (a copy, launch or event failed).                       */
+size_t lpcoll_host_workspace_bytes(int nranks, size_t chunk, lpcoll_dtype dtype,
+                                   int block, int flat, int tree, int slots);
+int lpcoll_host_allreduce(const void *const *host_in, void *const *host_out_flat,
+                          void *const *host_out_tree, int nranks, size_t n,
+                          lpcoll_dtype dtype, int block, size_t chunk, int slots,
+                          void *workspace, size_t workspace_bytes,
+                          void *copy_in_stream, void *compute_stream,
+                          void *copy_out_stream);
+
 /* dda_flat_sim with block = 128 for callers that cannot allocate device
  * memory. The pages have no counterpart: this exists for users of the
  * library, not for the method. Some callers cannot provide the wire buffers

@@ -56,6 +56,11 @@ def lib():
         L.lp_quantize_fmt.argtypes = [vp, ci, sz, ci, ci, vp, vp, vp]
         L.lp_dequantize_fmt.argtypes = [vp, vp, sz, ci, ci, vp, ci, vp]
         L.lp_reduce_fmt.argtypes = [pp, pp, ci, sz, ci, ci, vp, ci, vp]
+        L.lpcoll_host_workspace_bytes.argtypes = [ci, sz, ci, ci, ci, ci, ci]
+        L.lpcoll_host_workspace_bytes.restype = sz
+        L.lpcoll_host_allreduce.argtypes = [pp, pp, pp, ci, sz, ci, ci, sz, ci, vp, sz,
+                                            vp, vp, vp]
+        L.lpcoll_host_allreduce.restype = ci
         for f in ("lp_quantize", "lp_dequantize", "lp_reduce", "dda_flat_sim",
                   "dda_tree_sim", "reduce_scatter_sim", "all_gather_sim",
                   "all_to_all_sim", "dda_flat_sim_noalloc", "lp_quantize_fmt",
@@ -379,3 +384,61 @@ def lp_reduce_fmt(codes, scales, out, block, fmt, stream=None):
     _check(lib().lp_reduce_fmt(ptr_array(cps), ptr_array(sps), len(cps), n, block, fmt,
                                op, dtype_code(out), _stream(stream)), "lp_reduce_fmt")
     return out
+
+
+def lpcoll_host_workspace_bytes(nranks, chunk, dtype, block, flat, tree, slots):
+    """Device workspace bytes lpcoll_host_allreduce needs (0 if invalid)."""
+    return lib().lpcoll_host_workspace_bytes(nranks, chunk, dtype, block, int(bool(flat)),
+                                             int(bool(tree)), slots)
+
+
+def raw_host_allreduce(in_ptrs, flat_ptrs, tree_ptrs, nranks, n, dtype, block, chunk,
+                       slots, ws_ptr, ws_bytes, s_in, s_cmp, s_out):
+    """lpcoll_host_allreduce with host pointers as ints; flat_ptrs / tree_ptrs
+    None to skip that allreduce."""
+    _check(lib().lpcoll_host_allreduce(
+        ptr_array(in_ptrs), ptr_array(flat_ptrs) if flat_ptrs is not None else None,
+        ptr_array(tree_ptrs) if tree_ptrs is not None else None, nranks, n, dtype, block,
+        chunk, slots, ws_ptr, ws_bytes, s_in, s_cmp, s_out), "lpcoll_host_allreduce")
+
+
+def _host(t, what, dtype, numel):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError("%s must be a host (CPU) torch.Tensor" % what)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (what, dtype, t.dtype))
+    if t.numel() < numel:
+        raise ValueError("%s holds %d elements, needs %d" % (what, t.numel(), numel))
+    return t.data_ptr()
+
+
+def lpcoll_host_allreduce(host_ins, host_out_flat=None, host_out_tree=None, block=BLOCK,
+                          chunk=1 << 22, slots=3, workspace=None, streams=None):
+    """Flat and / or tree allreduce of N host tensors into host tensors,
+    chunked through a device workspace with copies and kernels overlapped.
+    Returns when the results are in host memory. workspace: a CUDA uint8
+    tensor of at least lpcoll_host_workspace_bytes(...) bytes; streams: three
+    CUDA streams (copy in, compute, copy out)."""
+    torch = _torch()
+    N = len(host_ins)
+    n = host_ins[0].numel()
+    dt = host_ins[0].dtype
+    ip = [_host(t, "host_in[%d]" % r, dt, n) for r, t in enumerate(host_ins)]
+    fp = None if host_out_flat is None else [
+        _host(t, "host_out_flat[%d]" % r, dt, n) for r, t in enumerate(host_out_flat)]
+    tp = None if host_out_tree is None else [
+        _host(t, "host_out_tree[%d]" % r, dt, n) for r, t in enumerate(host_out_tree)]
+    need = lpcoll_host_workspace_bytes(N, chunk, dtype_code(host_ins[0]), block,
+                                       fp is not None, tp is not None, slots)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    wp = _need(workspace, "workspace", torch.uint8, need)
+    if streams is None:
+        streams = [torch.cuda.current_stream()] * 3
+    sp = [_stream(x) for x in streams]
+    raw_host_allreduce(ip, fp, tp, N, n, dtype_code(host_ins[0]), block, chunk, slots, wp,
+                       workspace.numel(), *sp)
+    return host_out_flat, host_out_tree

@@ -22,7 +22,8 @@ STAMP = os.path.join(BUILD, "stamp")
 
 SOURCES = ["lpcoll_api.cu", "lpcoll_codec.cu", "lpcoll_dda_f32.cu",
            "lpcoll_dda_bf16.cu", "lpcoll_scatter_f32.cu", "lpcoll_scatter_bf16.cu",
-           "lpcoll_gather.cu", "lpcoll_variants.cu", "lpcoll_noalloc.cu"]
+           "lpcoll_gather.cu", "lpcoll_variants.cu", "lpcoll_host.cu",
+           "lpcoll_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false / -prec-div=true / -ftz=false back up the explicit __f*_rn
 # intrinsics: every float operation of the kernels is one IEEE operation.

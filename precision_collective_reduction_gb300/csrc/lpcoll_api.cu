@@ -221,6 +221,8 @@ int check_common(int dtype, int nranks, int block)
 
 }  // namespace
 
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
+
 int wave_ctas(const void *kernel, size_t units, int cap)
 {
     const size_t need = (units + kWarpsPerCta - 1) / kWarpsPerCta;

@@ -249,6 +249,9 @@ cudaError_t launch_scatter(const DdaParams &p, int nranks, size_t n, bool lp,
               : launch_dda_mode<DT, kScatterExact>(p, nranks, n, stream);
 }
 
+// Remember e as this thread's lpcoll_last_cuda_error() (lpcoll_api.cu).
+void record_cuda_error(cudaError_t e);
+
 // Defined in lpcoll_dda_f32.cu / lpcoll_dda_bf16.cu (allreduce) and
 // lpcoll_scatter_f32.cu / lpcoll_scatter_bf16.cu (reduce-scatter).
 cudaError_t launch_dda_f32(const DdaParams &p, int nranks, size_t n, int mode,

@@ -175,3 +175,25 @@ def test_variant_validation(L):
     assert L.lp_reduce_fmt(two, two, 2, 10, 96, 1, A, 0, None) == UNSUP
     assert L.lp_reduce_fmt(arr(A, None), two, 2, 10, 64, 1, A, 0, None) == RANK
     assert L.lp_reduce_fmt(two, two, 2, 10, 64, 1, None, 0, None) == ARG
+
+
+def test_host_allreduce_validation(L):
+    # every call fails its checks before any copy, so the fake host and
+    # device addresses are never touched
+    two = arr(A, A)
+    ws = L.lpcoll_host_workspace_bytes(2, 1024, 0, 128, 1, 1, 3)
+    assert ws > 0 and L.lpcoll_host_workspace_bytes(2, 1024, 0, 128, 1, 1, 0) == 0
+    assert L.lpcoll_host_workspace_bytes(2, 1024, 0, 128, 1, 1, 2) < ws
+    f = L.lpcoll_host_allreduce
+    assert f(two, two, two, 2, 10, 4, 128, 1024, 3, A, ws, None, None, None) == ARG   # dtype
+    assert f(two, two, two, 0, 10, 0, 128, 1024, 3, A, ws, None, None, None) == ARG   # N
+    assert f(two, two, two, 2, 10, 0, 128, 1024, 9, A, ws, None, None, None) == ARG   # slots
+    assert f(two, two, two, 2, 10, 0, 64, 1024, 3, A, ws, None, None, None) == UNSUP  # block
+    assert f(two, two, two, 2, 10, 0, 128, 1000, 3, A, ws, None, None, None) == ARG   # chunk
+    assert f(two, two, two, 2, 0, 0, 128, 1024, 3, A, ws, None, None, None) == OK     # n == 0
+    assert f(two, None, None, 2, 10, 0, 128, 1024, 3, A, ws, None, None, None) == ARG  # no output
+    assert f(two, two, None, 2, 10, 0, 128, 1024, 3, None, ws, None, None, None) == ARG
+    assert f(arr(A, None), two, None, 2, 10, 0, 128, 1024, 3, A, ws, None, None, None) == RANK
+    assert f(two, two, arr(None, A), 2, 10, 0, 128, 1024, 3, A, ws, None, None, None) == RANK
+    assert f(two, two, two, 2, 10, 0, 128, 1024, 3, A + 16, ws, None, None, None) == ALIGN
+    assert f(two, two, two, 2, 10, 0, 128, 1024, 3, A, ws - 1, None, None, None) == ARG

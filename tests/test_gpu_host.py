@@ -1,5 +1,6 @@
-"""HostAllreduce (host-resident buffers, chunked and overlapped) gives the
-same bits as one launch over the whole message, and as the oracle."""
+"""lpcoll_host_allreduce (host-resident buffers, chunked and overlapped,
+through HostAllreduce and directly) gives the same bits as one launch over
+the whole message, and as the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -45,7 +46,6 @@ def test_chunked_equals_single_launch(dt, block, chunk, slots):
             for t in hout[a]:
                 t.fill_(0)
         h.run(hin, hout)
-        h.synchronize()
         for r in range(N):
             assert same_bits(_np(hout["flat"][r], dt), from_dev(ref.outs[r]))
             assert same_bits(_np(hout["tree"][r], dt), from_dev(ref.tree_outs[r]))
@@ -57,7 +57,20 @@ def test_matches_oracle(oracle):
     h = HostAllreduce(N, n, W.F32, 128, algos=("tree",), chunk=128 * 32)
     hout = {"tree": [torch.empty(n, dtype=torch.float32).pin_memory() for _ in range(N)]}
     h.run([_host(x, W.F32) for x in ins], hout)
-    h.synchronize()
     want = oracle.tree(ins)[0]
     for r in range(N):
         assert same_bits(hout["tree"][r].numpy(), want[r])
+
+
+def test_direct_call_pageable_and_default_streams(oracle):
+    # pageable host memory and one stream for all three roles: no overlap,
+    # same results
+    import precision_collective_reduction_gb300 as pcr
+    N, n = 3, 128 * 77 + 9
+    ins = W.random_inputs(N, n, W.BF16, 8, scale_spread=2.0)
+    hin = [torch.from_numpy(x).view(torch.int16).view(torch.bfloat16) for x in ins]
+    hflat = [torch.empty(n, dtype=torch.bfloat16) for _ in range(N)]
+    pcr.lpcoll_host_allreduce(hin, host_out_flat=hflat, block=128, chunk=128 * 10, slots=2)
+    want = oracle.flat(ins)[0]
+    for r in range(N):
+        assert same_bits(_np(hflat[r], W.BF16), want[r])
