@@ -293,22 +293,25 @@ def e2e_steps(torch, w, steps, host_in, host_out, chunk):
     library's host-buffer entry point (lpcoll_host_allreduce, via
     HostAllreduce): per step, the host->device copies of the inputs, both
     allreduces and the device->host copies of both results, overlapped by
-    chunk. Each call returns once its results are in host memory; the events
-    bracket the calls on the first and last stream they use."""
+    chunk. Each call returns once its results are in host memory; a pair of
+    events brackets every call on the first and last stream it uses.
+    Returns (total ms, per-step ms list, kernel launches per step)."""
     from precision_collective_reduction_gb300.host import HostAllreduce
     h = HostAllreduce(w.nranks, w.n, w.dtype, w.block, algos=w.algos, chunk=chunk)
     h.run(host_in, host_out)          # warm-up pass
     torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(h.streams[0])
-    for _ in range(steps):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        a.record(h.streams[0])
         h.run(host_in, host_out)
-    end.record(h.streams[2])
-    end.synchronize()
+        b.record(h.streams[2])
+    ev[-1][1].synchronize()
+    per_step = [a.elapsed_time(b) for a, b in ev]
+    total = ev[0][0].elapsed_time(ev[-1][1])
     launches = h.kernel_launches_per_run()
     del h
-    return start.elapsed_time(end), launches
+    return total, per_step, launches
 
 
 def flush_l2(torch, scratch):
@@ -509,6 +512,7 @@ def run_ours(args):
     clocks = ClockSampler(local)
     total_ms, per_kernel, (t0, t1) = timed_steps(torch, bufs, w, stream, args.steps,
                                                  args.warmup, dist, clocks)
+    clocks.stop()  # samples are needed for the timed region only
     clock_info = clocks.summary(t0, t1)
     total_ms = max_over_ranks(total_ms, dist, "cuda")
     sbytes = step_bytes(w)
@@ -540,7 +544,8 @@ def run_ours(args):
     host_out = {a: [torch.empty(w.n, dtype=torch.float32).pin_memory()
                     for _ in range(w.nranks)] for a in w.algos}
     e2e_n = min(args.steps, E2E_MAX_STEPS)
-    e2e_ms, e2e_launches = e2e_steps(torch, w, e2e_n, host_in, host_out, E2E_CHUNK)
+    e2e_ms, e2e_per_step, e2e_launches = e2e_steps(torch, w, e2e_n, host_in, host_out,
+                                                    E2E_CHUNK)
     e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
     h2d = sum(x.nbytes for x in host)
     d2h = sum(h.numel() * h.element_size() for a in w.algos for h in host_out[a])
@@ -550,6 +555,10 @@ def run_ours(args):
            "api": "lpcoll_host_allreduce via HostAllreduce.run (chunks of %d "
                   "elements, copies and kernels overlapped on three streams)" % E2E_CHUNK,
            "kernel_launches_per_step": e2e_launches,
+           "ms_per_step_median": round(statistics.median(e2e_per_step), 3),
+           "ms_per_step_max": round(max(e2e_per_step), 3),
+           "note": "mean over the steps; single steps are sometimes delayed "
+                   "by host-side stalls of this shared machine (see the max)",
            "transfer_GBps": round((h2d + d2h) / (e2e_ms / e2e_n / 1e3) / 1e9, 1)}
     del host_in, host_out
     torch.cuda.empty_cache()
@@ -564,7 +573,6 @@ def run_ours(args):
                        W.LP_TREE_N8_64MB_BF16)}
         extras["collectives_lp_n8_16MiB_bf16"] = measure_collectives(torch, stream)
         extras["ablation_fp8_block"] = measure_variants(torch, stream)
-    clocks.stop()
 
     if rank != 0:
         return 0
