@@ -491,7 +491,10 @@ def run_ours(args):
     import torch
     rank, world, local = dist_env()
     dist = None
-    if world > 1:
+    if world > 1 or "TORCHELASTIC_RUN_ID" in os.environ:
+        # under torchrun (even with one rank) every rank joins the process
+        # group: a barrier brackets the timed steps and the slowest rank's
+        # time is the job's
         import torch.distributed as tdist
         torch.cuda.set_device(local)
         tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
