@@ -84,6 +84,24 @@ def dist_env():
     return rank, world, local
 
 
+class _StdoutToStderr:
+    """Send file descriptor 1 to stderr inside the block, so that libraries
+    that print to stdout (NCCL's version banner at communicator creation)
+    leave the benchmark's one JSON line alone."""
+
+    def __enter__(self):
+        sys.stdout.flush()
+        self.saved = os.dup(1)
+        os.dup2(2, 1)
+        return self
+
+    def __exit__(self, *exc):
+        sys.stdout.flush()
+        os.dup2(self.saved, 1)
+        os.close(self.saved)
+        return False
+
+
 def max_over_ranks(x, dist, device):
     """Largest value of x over all ranks (x itself when not distributed)."""
     if dist is None:
@@ -497,7 +515,9 @@ def run_ours(args):
         # time is the job's
         import torch.distributed as tdist
         torch.cuda.set_device(local)
-        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        with _StdoutToStderr():
+            tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+            tdist.barrier()
         dist = tdist
     else:
         torch.cuda.set_device(0)

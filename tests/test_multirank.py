@@ -55,3 +55,11 @@ def test_single_rank_defaults(monkeypatch):
         monkeypatch.delenv(k, raising=False)
     assert bench.dist_env() == (0, 1, 0)
     assert bench.max_over_ranks(3.5, None, "cpu") == 3.5
+
+
+def test_stdout_redirect_keeps_fd1_clean(capfd):
+    with bench._StdoutToStderr():
+        os.write(1, b"banner\n")
+    os.write(1, b"json\n")
+    out, err = capfd.readouterr()
+    assert out == "json\n" and "banner" in err
