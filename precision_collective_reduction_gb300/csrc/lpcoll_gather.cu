@@ -118,15 +118,27 @@ __device__ __forceinline__ void alltoall_item(const DdaParams &p, size_t c, size
         raw[k] = cnt[k] > 0 ? load_vec<DT>(p.in[r], src + e0[k], access_count<DT>(cnt[k], ALIGNED))
                             : make_uint4(0u, 0u, 0u, 0u);
     }
-    float x[kItemUnits][V];
-    encode_item<DT, LP>(p, r, src, static_cast<size_t>(j) * nbc, e0, cnt, raw, ALIGNED,
-                        lane, x);
+    // with every load issued, each unit goes all the way to its output before
+    // the next one is widened (fewer live registers than holding all units)
     const size_t at = static_cast<size_t>(r) * c;
 #pragma unroll
-    for (int k = 0; k < kItemUnits; ++k)
+    for (int k = 0; k < kItemUnits; ++k) {
+        float x[V];
+        widen<DT>(raw[k], x);
+        if constexpr (LP) {
+            float s;
+            const Codes<DT> cd = quantize_lane<DT>(x, s);
+            if (cnt[k] > 0) {
+                store_codes(p.codes[r], src + e0[k], access_count<DT>(cnt[k], ALIGNED), cd);
+                if ((lane % Fmt<DT>::kGroup) == 0)
+                    __stcs(p.scales[r] + static_cast<size_t>(j) * nbc + e0[k] / kBlock, s);
+            }
+            dequantize_lane<DT>(cd, s, x);
+        }
         if (cnt[k] > 0)
             store_vec<DT>(p.out[j], at + e0[k], access_count<DT>(cnt[k], ALIGNED),
-                          narrow<DT>(x[k]));
+                          narrow<DT>(x));
+    }
 }
 
 // At most 64 registers so that 4 CTAs fit per SM (7-9% faster than the 3
