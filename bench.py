@@ -453,6 +453,69 @@ def measure_collectives(torch, stream, iters=20):
     return out
 
 
+def staged_bytes(kind, N, n, elem):
+    """Algorithmic bytes of the staged building blocks: lp_quantize of one
+    rank (n s read, n q written), lp_dequantize (n q read, n s written),
+    lp_reduce of N payloads (N n q read, n s written)."""
+    q = n + 4 * ((n + 127) // 128)
+    if kind == "lp_quantize":
+        return n * elem + q
+    if kind == "lp_dequantize":
+        return q + n * elem
+    return N * q + n * elem
+
+
+def measure_staged(torch, stream, iters=10):
+    """lp_quantize, lp_dequantize and lp_reduce on the headline workload (8 x
+    64 Mi FP32) and on 8 x 16 MiB BF16, L2 flushed before each call."""
+    import precision_collective_reduction_gb300 as pcr
+    scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    res = {}
+    for w in (HEADLINE, W.LP_FLAT_N8_16MB_BF16):
+        N, n = w.nranks, w.n
+        tdt = torch.float32 if w.dtype == W.F32 else torch.bfloat16
+        ins = []
+        for x in W.draw_all(w):
+            t = torch.from_numpy(x)
+            ins.append((t.view(torch.int16).view(torch.bfloat16) if w.dtype == W.BF16
+                        else t).cuda())
+        codes = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(N)]
+        scales = [torch.empty(pcr.nblocks(n), dtype=torch.float32, device="cuda")
+                  for _ in range(N)]
+        for r in range(N):
+            pcr.lp_quantize(ins[r], codes[r], scales[r], stream=stream)
+        out = torch.empty(n, dtype=tdt, device="cuda")
+        calls = {
+            "lp_quantize": lambda: pcr.lp_quantize(ins[0], codes[0], scales[0], stream=stream),
+            "lp_dequantize": lambda: pcr.lp_dequantize(codes[0], scales[0], out, stream=stream),
+            "lp_reduce": lambda: pcr.lp_reduce(codes, scales, out, stream=stream),
+        }
+        row = {}
+        for kind, fn in calls.items():
+            for _ in range(3):
+                fn()
+            times = []
+            with torch.cuda.stream(stream):
+                for _ in range(iters):
+                    flush_l2(torch, scratch)
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    fn()
+                    b.record(stream)
+                    b.synchronize()
+                    times.append(a.elapsed_time(b) * 1e3)
+            us = statistics.median(times)
+            nbytes = staged_bytes(kind, N, n, w.elem_bytes)
+            row[kind] = {"us": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+                         "bytes_alg": nbytes}
+        res[w.name] = row
+        del ins, codes, scales, out
+        torch.cuda.empty_cache()
+    del scratch
+    return res
+
+
 def measure_variants(torch, stream, n=1 << 22, iters=10):
     """Ablation of the FP8 format and block size (staged path: quantize each
     of 8 ranks, then reduce), on the gradient workload's recipe at n elements
@@ -596,6 +659,7 @@ def run_ours(args):
                        W.LP_TREE_N8_64MB_BF16)}
         extras["collectives_lp_n8_16MiB_bf16"] = measure_collectives(torch, stream)
         extras["ablation_fp8_block"] = measure_variants(torch, stream)
+        extras["staged"] = measure_staged(torch, stream)
 
     if rank != 0:
         return 0

@@ -68,3 +68,11 @@ def test_collective_bytes():
     assert bench.collective_bytes("all_gather", N, m, 2, 128) == \
         N * m * 2 + N * (m + 4 * m // 128) + N * N * m * 2
     assert bench.collective_bytes("all_to_all", N, m, 2, 0) == 2 * N * N * m * 2
+
+
+def test_staged_bytes():
+    n, N = 128 * 1000, 8
+    q = n + 4 * 1000
+    assert bench.staged_bytes("lp_quantize", N, n, 4) == 4 * n + q
+    assert bench.staged_bytes("lp_dequantize", N, n, 2) == q + 2 * n
+    assert bench.staged_bytes("lp_reduce", N, n, 4) == N * q + 4 * n
