@@ -8,122 +8,155 @@
 
 namespace lpc {
 
-template <int DT, bool FULL>
-__device__ __forceinline__ void quantize_unit(const void *in, uint8_t *codes,
-                                              float *scales, size_t n, size_t unit,
-                                              int lane)
+// Units per loop iteration; all loads of an iteration are issued before any
+// of its units is processed. Measured on GB300 (8 x 64 Mi FP32): quantize
+// and dequantize gain 52% with 4 units over 1 (8 units: slower), the 8-rank
+// reduce 15% with 2 (4 units: its 16+ loads per unit spill, -40%).
+constexpr int kQuantizeUnits = 4;
+constexpr int kDequantizeUnits = 4;
+constexpr int kReduceUnits = 2;
+// The quantize kernel reads much more than it writes and takes all the
+// resident CTAs it can get (8 per SM: +10% over 4).
+constexpr int kQuantizeCtasPerSm = 8;
+
+// Warp-units [u0, u0 + K) of one message of n elements; e0 / cnt per lane.
+template <int DT, int K>
+__device__ __forceinline__ void unit_lanes(size_t n, size_t u0, int lane, size_t (&e0)[K],
+                                           int (&cnt)[K])
 {
-    constexpr int V = Fmt<DT>::kVec;
-    const size_t e0 = (unit * 32 + lane) * V;
-    const int cnt = FULL ? V : lane_count<DT>(n, e0);
-    const uint4 raw = (FULL || cnt > 0) ? load_vec<DT>(in, e0, cnt)
-                                        : make_uint4(0u, 0u, 0u, 0u);
-    float x[V];
-    widen<DT>(raw, x);
-    float s;
-    Codes<DT> c = quantize_lane<DT>(x, s);
-    if (FULL || cnt > 0) {
-        store_codes(codes, e0, cnt, c);
-        if ((lane % Fmt<DT>::kGroup) == 0)
-            __stcs(scales + e0 / kBlock, s);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        e0[k] = ((u0 + k) * 32 + lane) * Fmt<DT>::kVec;
+        cnt[k] = lane_count<DT>(n, e0[k]);
     }
 }
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads)
-quantize_kernel(const void *in, uint8_t *codes, float *scales, size_t n,
-                size_t full_units, size_t total_units)
+quantize_kernel(const void *in, uint8_t *codes, float *scales, size_t n, size_t items)
 {
+    constexpr int K = kQuantizeUnits;
+    constexpr int V = Fmt<DT>::kVec;
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
-    for (size_t u = warp; u < full_units; u += nwarps)
-        quantize_unit<DT, true>(in, codes, scales, n, u, lane);
-    if (total_units > full_units && warp == full_units % nwarps)
-        quantize_unit<DT, false>(in, codes, scales, n, full_units, lane);
-}
-
-template <int DT, bool FULL>
-__device__ __forceinline__ void dequantize_unit(const uint8_t *codes,
-                                                const float *scales, void *out,
-                                                size_t n, size_t unit, int lane)
-{
-    constexpr int V = Fmt<DT>::kVec;
-    const size_t e0 = (unit * 32 + lane) * V;
-    const int cnt = FULL ? V : lane_count<DT>(n, e0);
-    if (!FULL && cnt == 0)
-        return;
-    const Codes<DT> c = load_codes<DT>(codes, e0, cnt);
-    const float s = scales[e0 / kBlock];
-    float v[V];
-    dequantize_lane<DT>(c, s, v);
-    store_vec<DT>(out, e0, cnt, narrow<DT>(v));
+    for (size_t it = warp; it < items; it += nwarps) {
+        size_t e0[K];
+        int cnt[K];
+        unit_lanes<DT, K>(n, it * K, lane, e0, cnt);
+        uint4 raw[K];
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+            raw[k] = cnt[k] > 0 ? load_vec<DT>(in, e0[k], cnt[k]) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            float x[V];
+            widen<DT>(raw[k], x);
+            float s;
+            const Codes<DT> c = quantize_lane<DT>(x, s);
+            if (cnt[k] > 0) {
+                store_codes(codes, e0[k], cnt[k], c);
+                if ((lane % Fmt<DT>::kGroup) == 0)
+                    __stcs(scales + e0[k] / kBlock, s);
+            }
+        }
+    }
 }
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads)
 dequantize_kernel(const uint8_t *codes, const float *scales, void *out, size_t n,
-                  size_t full_units, size_t total_units)
+                  size_t items)
 {
+    constexpr int K = kDequantizeUnits;
+    constexpr int V = Fmt<DT>::kVec;
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
-    for (size_t u = warp; u < full_units; u += nwarps)
-        dequantize_unit<DT, true>(codes, scales, out, n, u, lane);
-    if (total_units > full_units && warp == full_units % nwarps)
-        dequantize_unit<DT, false>(codes, scales, out, n, full_units, lane);
-}
-
-template <int N, int DT, bool FULL>
-__device__ __forceinline__ void reduce_unit(const ReduceParams &p, void *out,
-                                            size_t n, size_t unit, int lane)
-{
-    constexpr int V = Fmt<DT>::kVec;
-    const size_t e0 = (unit * 32 + lane) * V;
-    const int cnt = FULL ? V : lane_count<DT>(n, e0);
-    if (!FULL && cnt == 0)
-        return;
-    Codes<DT> c[N];
-    float s[N];
+    for (size_t it = warp; it < items; it += nwarps) {
+        size_t e0[K];
+        int cnt[K];
+        unit_lanes<DT, K>(n, it * K, lane, e0, cnt);
+        Codes<DT> c[K];
+        float s[K];
 #pragma unroll
-    for (int r = 0; r < N; ++r) {
-        c[r] = load_codes<DT>(p.codes[r], e0, cnt);
-        s[r] = p.scales[r][e0 / kBlock];
+        for (int k = 0; k < K; ++k) {
+            if (cnt[k] > 0) {
+                c[k] = load_codes<DT>(codes, e0[k], cnt[k]);
+                s[k] = scales[e0[k] / kBlock];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            if (cnt[k] > 0) {
+                float v[V];
+                dequantize_lane<DT>(c[k], s[k], v);
+                store_vec<DT>(out, e0[k], cnt[k], narrow<DT>(v));
+            }
+        }
     }
-    float acc[V];
-#pragma unroll
-    for (int r = 0; r < N; ++r) {
-        float v[V];
-        dequantize_lane<DT>(c[r], s[r], v);
-#pragma unroll
-        for (int j = 0; j < V; ++j)
-            acc[j] = (r == 0) ? v[j] : __fadd_rn(acc[j], v[j]);
-    }
-    store_vec<DT>(out, e0, cnt, narrow<DT>(acc));
 }
 
 template <int N, int DT>
 __global__ void __launch_bounds__(kThreads)
-reduce_kernel(const __grid_constant__ ReduceParams p, void *out, size_t n,
-              size_t full_units, size_t total_units)
+reduce_kernel(const __grid_constant__ ReduceParams p, void *out, size_t n, size_t items)
 {
+    constexpr int K = kReduceUnits;
+    constexpr int V = Fmt<DT>::kVec;
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
-    for (size_t u = warp; u < full_units; u += nwarps)
-        reduce_unit<N, DT, true>(p, out, n, u, lane);
-    if (total_units > full_units && warp == full_units % nwarps)
-        reduce_unit<N, DT, false>(p, out, n, full_units, lane);
+    for (size_t it = warp; it < items; it += nwarps) {
+        size_t e0[K];
+        int cnt[K];
+        unit_lanes<DT, K>(n, it * K, lane, e0, cnt);
+        Codes<DT> c[K][N];
+        float s[K][N];
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            if (cnt[k] > 0) {
+#pragma unroll
+                for (int r = 0; r < N; ++r) {
+                    c[k][r] = load_codes<DT>(p.codes[r], e0[k], cnt[k]);
+                    s[k][r] = p.scales[r][e0[k] / kBlock];
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            if (cnt[k] > 0) {
+                float acc[V];
+#pragma unroll
+                for (int r = 0; r < N; ++r) {
+                    float v[V];
+                    dequantize_lane<DT>(c[k][r], s[k][r], v);
+#pragma unroll
+                    for (int j = 0; j < V; ++j)
+                        acc[j] = (r == 0) ? v[j] : __fadd_rn(acc[j], v[j]);
+                }
+                store_vec<DT>(out, e0[k], cnt[k], narrow<DT>(acc));
+            }
+        }
+    }
+}
+
+// Items of K warp-units covering a message of n elements.
+template <int DT, int K>
+inline size_t items_of(size_t n)
+{
+    size_t full, units;
+    unit_counts<DT>(n, full, units);
+    return (units + K - 1) / K;
 }
 
 template <int DT>
 cudaError_t launch_quantize_t(const void *in, uint8_t *codes, float *scales,
                               size_t n, cudaStream_t stream)
 {
-    size_t full, total;
-    unit_counts<DT>(n, full, total);
-    const int grid = wave_ctas(reinterpret_cast<const void *>(&quantize_kernel<DT>), total);
-    quantize_kernel<DT><<<grid, kThreads, 0, stream>>>(in, codes, scales, n, full, total);
+    const size_t items = items_of<DT, kQuantizeUnits>(n);
+    const int grid = wave_ctas(reinterpret_cast<const void *>(&quantize_kernel<DT>), items,
+                               kQuantizeCtasPerSm);
+    quantize_kernel<DT><<<grid, kThreads, 0, stream>>>(in, codes, scales, n, items);
     return cudaGetLastError();
 }
 
@@ -131,12 +164,10 @@ template <int DT>
 cudaError_t launch_dequantize_t(const uint8_t *codes, const float *scales, void *out,
                                 size_t n, cudaStream_t stream)
 {
-    size_t full, total;
-    unit_counts<DT>(n, full, total);
+    const size_t items = items_of<DT, kDequantizeUnits>(n);
     const int grid =
-        wave_ctas(reinterpret_cast<const void *>(&dequantize_kernel<DT>), total);
-    dequantize_kernel<DT><<<grid, kThreads, 0, stream>>>(codes, scales, out, n, full,
-                                                         total);
+        wave_ctas(reinterpret_cast<const void *>(&dequantize_kernel<DT>), items);
+    dequantize_kernel<DT><<<grid, kThreads, 0, stream>>>(codes, scales, out, n, items);
     return cudaGetLastError();
 }
 
@@ -144,11 +175,10 @@ template <int N, int DT>
 cudaError_t launch_reduce_n(const ReduceParams &p, void *out, size_t n,
                             cudaStream_t stream)
 {
-    size_t full, total;
-    unit_counts<DT>(n, full, total);
+    const size_t items = items_of<DT, kReduceUnits>(n);
     const int grid =
-        wave_ctas(reinterpret_cast<const void *>(&reduce_kernel<N, DT>), total);
-    reduce_kernel<N, DT><<<grid, kThreads, 0, stream>>>(p, out, n, full, total);
+        wave_ctas(reinterpret_cast<const void *>(&reduce_kernel<N, DT>), items);
+    reduce_kernel<N, DT><<<grid, kThreads, 0, stream>>>(p, out, n, items);
     return cudaGetLastError();
 }
 
