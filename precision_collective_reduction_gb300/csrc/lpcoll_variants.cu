@@ -11,7 +11,8 @@
 //
 // Work decomposition: a warp-unit is 32 lanes x 16 bytes (kVec elements per
 // lane), so a block spans block / kVec lanes; FP32 blocks of 256 span two
-// units, which one warp then processes together (U = 2).
+// units, which one warp then processes together (U = 2). A warp takes 4
+// consecutive units per iteration, all loads first.
 #include "lpcoll_dda.cuh"
 #include "lpcoll_device.cuh"
 
@@ -98,44 +99,56 @@ __device__ __forceinline__ void decode_lane(Codes<DT> c, float s,
     }
 }
 
-// Quantize U consecutive units of one message: a block covers G lanes of one
-// unit (U = 1) or both units (U = 2, FP32 blocks of 256).
+// Units per loop iteration of the quantize / dequantize variants; all their
+// loads are issued before any unit is processed (as in lp_quantize).
+constexpr int kVariantUnits = 4;
+
+// Quantize kVariantUnits consecutive units per iteration. A block covers G
+// lanes of one unit (U = 1) or the whole of two units (U = 2: FP32 blocks of
+// 256 elements); U divides kVariantUnits, so no block straddles iterations.
 template <int DT, int FMT, int U>
 __global__ void __launch_bounds__(kThreads)
 quantize_fmt_kernel(const void *in, uint8_t *codes, float *scales, size_t n, int block,
-                    size_t items)
+                    size_t groups)
 {
     constexpr int V = Fmt<DT>::kVec;
+    constexpr int K = kVariantUnits;
     const int lane = threadIdx.x & 31;
     const int G = (U == 2) ? 32 : block / V;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
-    for (size_t it = warp; it < items; it += nwarps) {
-        size_t e0[U];
-        int cnt[U];
-        float x[U][V];
-        float amax = 0.0f;
+    for (size_t g = warp; g < groups; g += nwarps) {
+        size_t e0[K];
+        int cnt[K];
+        uint4 raw[K];
 #pragma unroll
-        for (int k = 0; k < U; ++k) {
-            e0[k] = ((it * U + k) * 32 + lane) * V;
+        for (int k = 0; k < K; ++k) {
+            e0[k] = ((g * K + k) * 32 + lane) * V;
             cnt[k] = lane_count<DT>(n, e0[k]);
-            const uint4 raw = cnt[k] > 0 ? load_vec<DT>(in, e0[k], cnt[k])
-                                         : make_uint4(0u, 0u, 0u, 0u);
-            widen<DT>(raw, x[k]);
-            float a = 0.0f;
-#pragma unroll
-            for (int j = 0; j < V; ++j)
-                a = fmaxf(a, fabsf(x[k][j]));
-            amax = fmaxf(amax, group_max_rt(a, G));
+            raw[k] = cnt[k] > 0 ? load_vec<DT>(in, e0[k], cnt[k]) : make_uint4(0u, 0u, 0u, 0u);
         }
-        float s, inv;
-        block_scale_fmt<FMT>(amax, s, inv);
 #pragma unroll
-        for (int k = 0; k < U; ++k) {
-            if (cnt[k] > 0) {
-                store_codes(codes, e0[k], cnt[k], encode_lane<DT, FMT>(x[k], inv));
-                if (k == 0 && (lane % G) == 0)
-                    scales[e0[k] / block] = s;
+        for (int i = 0; i < K; i += U) {
+            float x[U][V];
+            float amax = 0.0f;
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                widen<DT>(raw[i + k], x[k]);
+                float a = 0.0f;
+#pragma unroll
+                for (int j = 0; j < V; ++j)
+                    a = fmaxf(a, fabsf(x[k][j]));
+                amax = fmaxf(amax, group_max_rt(a, G));
+            }
+            float s, inv;
+            block_scale_fmt<FMT>(amax, s, inv);
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                if (cnt[i + k] > 0) {
+                    store_codes(codes, e0[i + k], cnt[i + k], encode_lane<DT, FMT>(x[k], inv));
+                    if (k == 0 && (lane % G) == 0)
+                        scales[e0[i] / block] = s;
+                }
             }
         }
     }
@@ -144,20 +157,35 @@ quantize_fmt_kernel(const void *in, uint8_t *codes, float *scales, size_t n, int
 template <int DT, int FMT>
 __global__ void __launch_bounds__(kThreads)
 dequantize_fmt_kernel(const uint8_t *codes, const float *scales, void *out, size_t n,
-                      int block, size_t units)
+                      int block, size_t groups)
 {
     constexpr int V = Fmt<DT>::kVec;
+    constexpr int K = kVariantUnits;
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
-    for (size_t u = warp; u < units; u += nwarps) {
-        const size_t e0 = (u * 32 + lane) * V;
-        const int cnt = lane_count<DT>(n, e0);
-        if (cnt <= 0)
-            continue;
-        float v[V];
-        decode_lane<DT, FMT>(load_codes<DT>(codes, e0, cnt), scales[e0 / block], v);
-        store_vec<DT>(out, e0, cnt, narrow<DT>(v));
+    for (size_t g = warp; g < groups; g += nwarps) {
+        size_t e0[K];
+        int cnt[K];
+        Codes<DT> c[K];
+        float s[K];
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            e0[k] = ((g * K + k) * 32 + lane) * V;
+            cnt[k] = lane_count<DT>(n, e0[k]);
+            if (cnt[k] > 0) {
+                c[k] = load_codes<DT>(codes, e0[k], cnt[k]);
+                s[k] = scales[e0[k] / block];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            if (cnt[k] > 0) {
+                float v[V];
+                decode_lane<DT, FMT>(c[k], s[k], v);
+                store_vec<DT>(out, e0[k], cnt[k], narrow<DT>(v));
+            }
+        }
     }
 }
 
@@ -194,15 +222,15 @@ cudaError_t quantize_fmt_t(const void *in, size_t n, int block, uint8_t *codes,
 {
     size_t full, units;
     unit_counts<DT>(n, full, units);
+    const size_t groups = (units + kVariantUnits - 1) / kVariantUnits;
     if (block > 32 * Fmt<DT>::kVec) {  // FP32, block 256: two units per block
-        const size_t items = (units + 1) / 2;
         const void *k = reinterpret_cast<const void *>(&quantize_fmt_kernel<DT, FMT, 2>);
         quantize_fmt_kernel<DT, FMT, 2>
-            <<<wave_ctas(k, items), kThreads, 0, st>>>(in, codes, scales, n, block, items);
+            <<<wave_ctas(k, groups), kThreads, 0, st>>>(in, codes, scales, n, block, groups);
     } else {
         const void *k = reinterpret_cast<const void *>(&quantize_fmt_kernel<DT, FMT, 1>);
         quantize_fmt_kernel<DT, FMT, 1>
-            <<<wave_ctas(k, units), kThreads, 0, st>>>(in, codes, scales, n, block, units);
+            <<<wave_ctas(k, groups), kThreads, 0, st>>>(in, codes, scales, n, block, groups);
     }
     return cudaGetLastError();
 }
@@ -213,9 +241,10 @@ cudaError_t dequantize_fmt_t(const uint8_t *codes, const float *scales, size_t n
 {
     size_t full, units;
     unit_counts<DT>(n, full, units);
+    const size_t groups = (units + kVariantUnits - 1) / kVariantUnits;
     const void *k = reinterpret_cast<const void *>(&dequantize_fmt_kernel<DT, FMT>);
     dequantize_fmt_kernel<DT, FMT>
-        <<<wave_ctas(k, units), kThreads, 0, st>>>(codes, scales, out, n, block, units);
+        <<<wave_ctas(k, groups), kThreads, 0, st>>>(codes, scales, out, n, block, groups);
     return cudaGetLastError();
 }
 
