@@ -76,12 +76,24 @@ _default_ws = Workspace()
 
 def allreduce_sim(tensors, low_precision=None, algo="auto", stream=None,
                   workspace=None):
-    """SUM-allreduce the N rank tensors in place; returns (algo, block) used."""
+    """SUM-allreduce the N rank tensors in place; returns (algo, block) used.
+
+    CUDA tensors are reduced by one fused launch. Host (CPU) tensors, as in
+    the pages' example, go through the library's host-buffer pipeline
+    (lpcoll_host_allreduce): copied to the GPU chunk by chunk, reduced, and
+    written back in place; the call returns when they hold the result."""
     tensors = list(tensors)
     if not tensors:
         raise ValueError("need at least one rank tensor")
     n = tensors[0].numel()
     algo, block = choose(n * tensors[0].element_size(), low_precision, algo)
+    if not tensors[0].is_cuda:
+        chunk = 1 << 22
+        outs = {"flat": None, "tree": None}
+        outs[algo] = tensors
+        B.lpcoll_host_allreduce(tensors, outs["flat"], outs["tree"], block=block,
+                                chunk=chunk, slots=3)
+        return algo, block
     ws = None
     if block:
         ws = (workspace or _default_ws).get(tensors[0].device, len(tensors), n)

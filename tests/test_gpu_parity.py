@@ -275,3 +275,18 @@ def test_cuda_graph_replay(oracle, block):
     want = oracle.flat(ins, block=block)[0]
     for r in range(N):
         assert_same(from_dev(outs[r]), want[r], "out[%d]" % r)
+
+
+def test_pages_example_with_host_tensors():
+    # the example as the pages write it: torch.full on the host, SUM in place
+    from oracle_pins import read_torch_full_cases
+    for N, rows, cols, want in read_torch_full_cases():
+        ts = [torch.full((rows, cols), float(r), dtype=torch.float) for r in range(N)]
+        algo, block = pcr.allreduce_sim(ts)
+        assert (algo, block) == ("flat", 0)
+        for t in ts:
+            assert not t.is_cuda and torch.all(t == want).item(), (N, want)
+        ts = [torch.full((rows, cols), float(r), dtype=torch.bfloat16) for r in range(N)]
+        pcr.allreduce_sim(ts, algo="tree")
+        for t in ts:
+            assert torch.all(t.float() == want).item(), (N, want)
