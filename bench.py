@@ -37,8 +37,6 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-import numpy as np  # noqa: E402
-
 from precision_collective_reduction_gb300 import workloads as W  # noqa: E402
 
 HEADLINE = W.LP_GRAD_N8_256MB_F32
@@ -160,7 +158,6 @@ class ClockSampler:
     def __init__(self, device_index):
         self.samples = []
         self.proc = None
-        self.marks = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(device_index), "--query-gpu=" + self.FIELDS,
@@ -176,9 +173,6 @@ class ClockSampler:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 8:
                 self.samples.append((time.monotonic(), parts))
-
-    def mark(self):
-        self.marks.append(time.monotonic())
 
     def stop(self):
         if self.proc is not None:
@@ -278,7 +272,7 @@ def workload_config(w, world):
 
 # -- GPU legs -------------------------------------------------------------------
 
-def timed_steps(torch, bufs, w, stream, steps, warmup, dist, clocks):
+def timed_steps(torch, bufs, w, stream, steps, warmup, dist):
     s = stream.cuda_stream
     for _ in range(warmup):
         for a in w.algos:
@@ -597,7 +591,7 @@ def run_ours(args):
 
     clocks = ClockSampler(local)
     total_ms, per_kernel, (t0, t1) = timed_steps(torch, bufs, w, stream, args.steps,
-                                                 args.warmup, dist, clocks)
+                                                 args.warmup, dist)
     clocks.stop()  # samples are needed for the timed region only
     clock_info = clocks.summary(t0, t1)
     total_ms = max_over_ranks(total_ms, dist, "cuda")
