@@ -738,6 +738,25 @@ def _collective_runner(torch, bufs, kind):
                                            wire_scales=bufs.wire_scales, stream=s)
 
 
+def _staged_runner(torch, bufs, kind):
+    """run(algo, stream) for one staged building block over the buffers of a
+    RankBuffers (low precision): lp_quantize of rank 0's message, lp_dequantize
+    of rank 0's payload, or lp_reduce of all N payloads. The payloads are
+    filled once before the first call."""
+    import precision_collective_reduction_gb300 as pcr
+    s0 = torch.cuda.current_stream().cuda_stream
+    for r in range(bufs.nranks):
+        pcr.lp_quantize(bufs.ins[r], bufs.wire_codes[r], bufs.wire_scales[r], stream=s0)
+    if kind == "quantize":
+        return lambda a, s: pcr.lp_quantize(bufs.ins[0], bufs.wire_codes[0],
+                                            bufs.wire_scales[0], stream=s)
+    if kind == "dequantize":
+        return lambda a, s: pcr.lp_dequantize(bufs.wire_codes[0], bufs.wire_scales[0],
+                                              bufs.outs[0], stream=s)
+    return lambda a, s: pcr.lp_reduce(bufs.wire_codes, bufs.wire_scales, bufs.outs[0],
+                                      stream=s)
+
+
 def run_profile_case(args):
     """A few launches of one workload's kernels, for ncu captures: `warmup`
     untimed launches of each algorithm, then `steps` more."""
@@ -754,6 +773,8 @@ def run_profile_case(args):
     run = bufs.run
     if algos[0] in ("rs", "ag", "a2a"):
         run = _collective_runner(torch, bufs, algos[0])
+    elif algos[0] in ("quantize", "dequantize", "reduce"):
+        run = _staged_runner(torch, bufs, algos[0])
     for _ in range(args.warmup):
         for a in algos:
             run(a, s)
@@ -779,9 +800,10 @@ def main():
                     help="only run a few launches of this workload (for ncu)")
     ap.add_argument("--elems", type=int, default=0,
                     help="with --profile-case: elements per rank (default: full)")
-    ap.add_argument("--algo", choices=["flat", "tree", "rs", "ag", "a2a"], default=None,
-                    help="with --profile-case: the operation to run (rs, ag and a2a "
-                         "need a low-precision workload)")
+    ap.add_argument("--algo", choices=["flat", "tree", "rs", "ag", "a2a", "quantize",
+                                       "dequantize", "reduce"], default=None,
+                    help="with --profile-case: the operation to run (all but flat and "
+                         "tree need a low-precision workload)")
     ap.add_argument("--crossover", action="store_true",
                     help="only time flat vs tree over message sizes")
     args = ap.parse_args()
