@@ -767,7 +767,8 @@ def run_profile_case(args):
     w = W.BY_NAME[args.profile_case]
     n = args.elems or w.n
     algos = [args.algo] if args.algo else list(w.algos)
-    bufs = runner.RankBuffers(w.nranks, n, w.dtype, w.block, separate_tree_out=True)
+    bufs = runner.RankBuffers(w.nranks, n, w.dtype, w.block,
+                              separate_tree_out="tree" in algos)
     bufs.load(W.draw_all(w, n))
     s = torch.cuda.current_stream().cuda_stream
     run = bufs.run

@@ -120,7 +120,7 @@ def test_dequantize(oracle, dt, n):
 
 @pytest.mark.parametrize("dt", [F32, BF16])
 @pytest.mark.parametrize("N", [1, 2, 3, 8, 16])
-@pytest.mark.parametrize("n", [5, 200, 4096 + 77])
+@pytest.mark.parametrize("n", [5, 200, 511, 513, 4096 + 77, 128 * 37 + 15])
 def test_reduce(oracle, dt, N, n):
     ins = W.random_inputs(N, n, dt, 3000 + 31 * N + n, scale_spread=4.0)
     pays = [oracle.quantize(x) for x in ins]
@@ -130,6 +130,26 @@ def test_reduce(oracle, dt, N, n):
     assert out.intact()
     want = oracle.reduce([c for c, _ in pays], [s for _, s in pays], dtype=_np_dt(dt))
     assert_same(from_dev(out.t), want, "out")
+
+
+@pytest.mark.parametrize("dt", [F32, BF16])
+def test_staged_many_grid_passes(oracle, dt):
+    """lp_quantize and lp_reduce over a message long enough that every warp of
+    the launch takes several grid-stride passes, with a ragged tail inside one
+    lane's elements."""
+    N, n = 3, 11 * (1 << 20) + 333
+    ins = W.random_inputs(N, n, dt, 7100 + dt, scale_spread=5.0)
+    pays = [gpu_quantize(x) for x in ins]
+    want = [oracle.quantize(x) for x in ins]
+    for r in range(N):
+        assert_same(pays[r][0], want[r][0], "codes[%d]" % r)
+        assert_same(pays[r][1], want[r][1], "scales[%d]" % r)
+    out = Guarded(n, TORCH_DT[dt])
+    pcr.lp_reduce([to_dev(c) for c, _ in pays], [to_dev(s) for _, s in pays], out.t)
+    torch.cuda.synchronize()
+    assert out.intact()
+    assert_same(from_dev(out.t), oracle.reduce([c for c, _ in want], [s for _, s in want],
+                                               dtype=_np_dt(dt)), "out")
 
 
 # -- fused allreduce ------------------------------------------------------------
