@@ -18,6 +18,7 @@
 // was no faster.
 #include "lpcoll_dda.cuh"
 #include "lpcoll_device.cuh"
+#include "lpcoll_wide.cuh"
 
 namespace lpc {
 
@@ -28,11 +29,6 @@ constexpr int kDequantizeUnits = 4;
 // The quantize kernel reads four times what it writes and takes all the
 // resident CTAs it can get (up to 8 per SM: +10% over 4).
 constexpr int kQuantizeCtasPerSm = 8;
-// Wide layout: elements per lane, lanes per block, elements per warp item.
-constexpr int kWideElems = 16;
-constexpr int kWideGroup = kBlock / kWideElems;
-constexpr int kWideItem = 32 * kWideElems;
-
 // Warp-units [u0, u0 + K) of one message of n elements; e0 / cnt per lane.
 template <int DT, int K>
 __device__ __forceinline__ void unit_lanes(size_t n, size_t u0, int lane, size_t (&e0)[K],
@@ -43,87 +39,6 @@ __device__ __forceinline__ void unit_lanes(size_t n, size_t u0, int lane, size_t
         e0[k] = ((u0 + k) * 32 + lane) * Fmt<DT>::kVec;
         cnt[k] = lane_count<DT>(n, e0[k]);
     }
-}
-
-// 16 codes of a wide lane starting at element e0 < n (missing ones read 0).
-__device__ __forceinline__ uint4 wide_load_codes(const uint8_t *codes, size_t n, size_t e0)
-{
-    if (n - e0 >= kWideElems)
-        return __ldcs(reinterpret_cast<const uint4 *>(codes + e0));
-    const size_t c = n - e0;
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-    for (int j = 0; j < kWideElems; ++j)
-        if (static_cast<size_t>(j) < c)
-            w[j / 4] |= static_cast<uint32_t>(codes[e0 + j]) << (8 * (j % 4));
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Store the codes of a wide lane starting at element e0 < n.
-__device__ __forceinline__ void wide_store_codes(uint8_t *codes, size_t n, size_t e0,
-                                                 const uint32_t (&w)[4])
-{
-    if (n - e0 >= kWideElems) {
-        __stcs(reinterpret_cast<uint4 *>(codes + e0), make_uint4(w[0], w[1], w[2], w[3]));
-        return;
-    }
-    const size_t c = n - e0;
-#pragma unroll
-    for (int j = 0; j < kWideElems; ++j)
-        if (static_cast<size_t>(j) < c)
-            codes[e0 + j] = static_cast<uint8_t>(w[j / 4] >> (8 * (j % 4)));
-}
-
-// v = fl(e4m3(code) * s) for the 16 codes of a wide lane.
-__device__ __forceinline__ void wide_dequant(uint4 c, float s, float (&v)[kWideElems])
-{
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 lo = dec2(w[q]);
-        const float2 hi = dec2(w[q] >> 16);
-        v[4 * q + 0] = __fmul_rn(lo.x, s);
-        v[4 * q + 1] = __fmul_rn(lo.y, s);
-        v[4 * q + 2] = __fmul_rn(hi.x, s);
-        v[4 * q + 3] = __fmul_rn(hi.y, s);
-    }
-}
-
-// Store the 16 results of every lane of a warp item (first element item_e0)
-// through the warp's shared-memory stage, so that each global store
-// instruction writes 32 consecutive 16-byte vectors instead of 32 vectors
-// 64 (FP32) or 32 (BF16) bytes apart. The slot of a vector is XOR-swizzled
-// so that neither the writes nor the reads of the stage conflict on banks.
-// All 32 lanes call it; results of lanes past the end are not stored.
-template <int DT>
-__device__ __forceinline__ void wide_store_results(void *out, size_t n, size_t item_e0,
-                                                   const float (&v)[kWideElems],
-                                                   uint4 *stage, int lane)
-{
-    constexpr int V = Fmt<DT>::kVec;
-    constexpr int S = kWideElems / V;  // vectors per lane: 4 or 2
-#pragma unroll
-    for (int j = 0; j < S; ++j) {
-        float t[V];
-#pragma unroll
-        for (int i = 0; i < V; ++i)
-            t[i] = v[j * V + i];
-        const int x = S == 4 ? ((lane >> 1) & 3) : ((lane >> 2) & 1);
-        stage[lane * S + (j ^ x)] = narrow<DT>(t);
-    }
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < S; ++k) {
-        const int m = k * 32 + lane;  // vector m of the item, held by lane m / S
-        const int src = m / S;
-        const int x = S == 4 ? ((src >> 1) & 3) : ((src >> 2) & 1);
-        const uint4 val = stage[src * S + ((m % S) ^ x)];
-        const size_t e = item_e0 + static_cast<size_t>(m) * V;
-        const int cnt = lane_count<DT>(n, e);
-        if (cnt > 0)
-            store_vec<DT>(out, e, cnt, val);
-    }
-    __syncwarp();
 }
 
 template <int DT>
@@ -144,26 +59,10 @@ quantize_kernel(const void *in, uint8_t *codes, float *scales, size_t n, size_t 
             raw[j] = cnt > 0 ? load_vec<DT>(in, e0 + j * V, cnt) : make_uint4(0u, 0u, 0u, 0u);
         }
         float x[kWideElems];
-#pragma unroll
-        for (int j = 0; j < S; ++j) {
-            float t[V];
-            widen<DT>(raw[j], t);
-#pragma unroll
-            for (int i = 0; i < V; ++i)
-                x[j * V + i] = t[i];
-        }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kWideElems; ++i)
-            amax = fmaxf(amax, fabsf(x[i]));
-        amax = group_max<kWideGroup>(amax);
-        float s, inv;
-        block_scale(amax, s, inv);
+        wide_widen<DT>(raw, x);
+        float s;
         uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            w[q] = enc2(__fmul_rn(x[4 * q], inv), __fmul_rn(x[4 * q + 1], inv)) |
-                   (enc2(__fmul_rn(x[4 * q + 2], inv), __fmul_rn(x[4 * q + 3], inv)) << 16);
+        wide_quantize(x, w, s);
         if (e0 < n) {
             wide_store_codes(codes, n, e0, w);
             if (lane % kWideGroup == 0)

@@ -1,20 +1,27 @@
 // lpcoll_gather.cu -- the collectives without a reduction: AllGather and
 // AlltoAll over N emulated ranks, exact or low precision.
 //
-// Each warp takes an item of kItemUnits consecutive units (32 x kVec
-// elements each) of one sender's data: it loads them all, and in low
-// precision quantizes them on the sender's blocks (one absmax scale per 128
-// elements counted from the start of what the sender sends), stores the
-// codes and scales to the sender's wire payload, and dequantizes them in
-// registers; then it writes the (dequantized) values to the receiving
-// outputs. Warps stride over (sender, destination, item), so each sender's
-// data streams through HBM in order.
+// AllGather and the exact AlltoAll: each warp takes an item of kItemUnits
+// consecutive units (32 x kVec elements each) of one sender's data: it loads
+// them all, and in low precision quantizes them on the sender's blocks (one
+// absmax scale per 128 elements counted from the start of what the sender
+// sends), stores the codes and scales to the sender's wire payload, and
+// dequantizes them in registers; then it writes the (dequantized) values to
+// the receiving outputs. Warps stride over (sender, destination, item), so
+// each sender's data streams through HBM in order.
+//
+// The low-precision AlltoAll uses the wide lane layout (16 elements per lane,
+// 8 lanes per block, 512 elements per warp item; lpcoll_wide.cuh), with the
+// results written through the warp's shared-memory stage. On GB300 it took
+// the 8-rank all-to-all from 61.4 to 57.2 us (BF16, chunks of 1 Mi), 227.3 to
+// 214.7 us (BF16, 4 Mi) and 783.4 to 719.7 us (FP32, 8 Mi).
 //
 // Offsets that are not 16-byte aligned (a contribution or chunk length that
 // is not a multiple of 16 bytes) take the element-by-element path for the
 // accesses that need it; the choice is made once per launch (ALIGNED).
 #include "lpcoll_dda.cuh"
 #include "lpcoll_device.cuh"
+#include "lpcoll_wide.cuh"
 
 namespace lpc {
 
@@ -101,10 +108,10 @@ gather_kernel(const __grid_constant__ DdaParams p, int nranks, size_t m, size_t 
     }
 }
 
-// One item of chunk j (c elements) of sender r in the AlltoAll.
-template <int DT, bool LP, bool ALIGNED>
-__device__ __forceinline__ void alltoall_item(const DdaParams &p, size_t c, size_t nbc,
-                                              int r, int j, size_t g, int lane)
+// One item of chunk j (c elements) of sender r in the exact AlltoAll.
+template <int DT, bool ALIGNED>
+__device__ __forceinline__ void alltoall_item(const DdaParams &p, size_t c, int r, int j,
+                                              size_t g, int lane)
 {
     constexpr int V = Fmt<DT>::kVec;
     const size_t src = static_cast<size_t>(j) * c;
@@ -118,35 +125,16 @@ __device__ __forceinline__ void alltoall_item(const DdaParams &p, size_t c, size
         raw[k] = cnt[k] > 0 ? load_vec<DT>(p.in[r], src + e0[k], access_count<DT>(cnt[k], ALIGNED))
                             : make_uint4(0u, 0u, 0u, 0u);
     }
-    // with every load issued, each unit goes all the way to its output before
-    // the next one is widened (fewer live registers than holding all units)
     const size_t at = static_cast<size_t>(r) * c;
 #pragma unroll
-    for (int k = 0; k < kItemUnits; ++k) {
-        float x[V];
-        widen<DT>(raw[k], x);
-        if constexpr (LP) {
-            float s;
-            const Codes<DT> cd = quantize_lane<DT>(x, s);
-            if (cnt[k] > 0) {
-                store_codes(p.codes[r], src + e0[k], access_count<DT>(cnt[k], ALIGNED), cd);
-                if ((lane % Fmt<DT>::kGroup) == 0)
-                    __stcs(p.scales[r] + static_cast<size_t>(j) * nbc + e0[k] / kBlock, s);
-            }
-            dequantize_lane<DT>(cd, s, x);
-        }
+    for (int k = 0; k < kItemUnits; ++k)
         if (cnt[k] > 0)
-            store_vec<DT>(p.out[j], at + e0[k], access_count<DT>(cnt[k], ALIGNED),
-                          narrow<DT>(x));
-    }
+            store_vec<DT>(p.out[j], at + e0[k], access_count<DT>(cnt[k], ALIGNED), raw[k]);
 }
 
-// At most 64 registers so that 4 CTAs fit per SM (7-9% faster than the 3
-// its unconstrained 74 registers allow).
-template <int DT, bool LP, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads, kCtasPerSmBusy)
-alltoall_kernel(const __grid_constant__ DdaParams p, int nranks, size_t c, size_t nbc,
-                size_t groups)
+template <int DT, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads)
+alltoall_kernel(const __grid_constant__ DdaParams p, int nranks, size_t c, size_t groups)
 {
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
@@ -157,8 +145,87 @@ alltoall_kernel(const __grid_constant__ DdaParams p, int nranks, size_t c, size_
         const int r = static_cast<int>(it / per_sender);
         const size_t rest = it - static_cast<size_t>(r) * per_sender;
         const int j = static_cast<int>(rest / groups);
-        alltoall_item<DT, LP, ALIGNED>(p, c, nbc, r, j, rest - static_cast<size_t>(j) * groups,
-                                       lane);
+        alltoall_item<DT, ALIGNED>(p, c, r, j, rest - static_cast<size_t>(j) * groups, lane);
+    }
+}
+
+// Low-precision AlltoAll, per element format: wide items per warp step (all
+// their loads issued first) and resident CTAs per SM. Measured on GB300 with
+// 8 ranks: FP32 1 item at 3 CTAs per SM (2 CTAs: -17%; 2 items: -1%), BF16
+// 2 items at 4 CTAs per SM (1 item: -20%; 4 items: -3%; 3 CTAs: -4%).
+template <int DT> struct A2aLp;
+template <> struct A2aLp<LPCOLL_F32> {
+    static constexpr int kItems = 1;
+    static constexpr int kCtas = 3;
+};
+template <> struct A2aLp<LPCOLL_BF16> {
+    static constexpr int kItems = 2;
+    static constexpr int kCtas = 4;
+};
+
+// One step of the low-precision AlltoAll: wide items [g K, (g+1) K) of chunk j
+// (c elements) of sender r. Each is quantized on the chunk's own blocks, its
+// codes and scale go to sender r's wire (scales of chunk j start at j nbc),
+// and the dequantized values go to out[j] at r c.
+template <int DT, bool ALIGNED>
+__device__ __forceinline__ void alltoall_lp_step(const DdaParams &p, size_t c, size_t nbc,
+                                                 int r, int j, size_t g, int lane,
+                                                 uint4 *stage)
+{
+    constexpr int V = Fmt<DT>::kVec;
+    constexpr int S = kWideElems / V;
+    constexpr int K = A2aLp<DT>::kItems;
+    constexpr int ES = 16 / V;
+    const size_t src = static_cast<size_t>(j) * c;
+    size_t e0[K];
+    uint4 raw[K][S];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        e0[k] = (g * K + k) * kWideItem + static_cast<size_t>(lane) * kWideElems;
+#pragma unroll
+        for (int q = 0; q < S; ++q) {
+            const size_t e = e0[k] + q * V;
+            const int cnt = lane_count<DT>(c, e);
+            raw[k][q] = cnt > 0 ? load_vec<DT>(p.in[r], src + e, access_count<DT>(cnt, ALIGNED))
+                                : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    char *out = static_cast<char *>(p.out[j]) + static_cast<size_t>(r) * c * ES;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        float x[kWideElems];
+        wide_widen<DT>(raw[k], x);
+        float s;
+        uint32_t w[4];
+        wide_quantize(x, w, s);
+        if (e0[k] < c) {
+            wide_store_codes(p.codes[r] + src, c, e0[k], w);
+            if (lane % kWideGroup == 0)
+                __stcs(p.scales[r] + static_cast<size_t>(j) * nbc + e0[k] / kBlock, s);
+        }
+        wide_dequant(make_uint4(w[0], w[1], w[2], w[3]), s, x);
+        wide_store_results<DT, ALIGNED>(out, c, (g * K + k) * kWideItem, x, stage, lane);
+    }
+}
+
+template <int DT, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads, A2aLp<DT>::kCtas)
+alltoall_lp_kernel(const __grid_constant__ DdaParams p, int nranks, size_t c, size_t nbc,
+                   size_t groups)
+{
+    __shared__ uint4 stage_all[kWarpsPerCta][kWideElems * 32 / 4];
+    uint4 *stage = stage_all[threadIdx.x >> 5];
+    const int lane = threadIdx.x & 31;
+    const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
+    const size_t per_sender = static_cast<size_t>(nranks) * groups;
+    const size_t items = static_cast<size_t>(nranks) * per_sender;
+    for (size_t it = warp; it < items; it += nwarps) {
+        const int r = static_cast<int>(it / per_sender);
+        const size_t rest = it - static_cast<size_t>(r) * per_sender;
+        const int j = static_cast<int>(rest / groups);
+        alltoall_lp_step<DT, ALIGNED>(p, c, nbc, r, j, rest - static_cast<size_t>(j) * groups,
+                                      lane, stage);
     }
 }
 
@@ -184,12 +251,20 @@ cudaError_t launch_gather_t(const DdaParams &p, int nranks, size_t m, cudaStream
 template <int DT, bool LP, bool ALIGNED>
 cudaError_t launch_alltoall_t(const DdaParams &p, int nranks, size_t c, cudaStream_t st)
 {
-    const size_t groups = item_groups<DT>(c);
-    const size_t nbc = (c + kBlock - 1) / kBlock;
-    const void *k = reinterpret_cast<const void *>(&alltoall_kernel<DT, LP, ALIGNED>);
-    const int grid =
-        wave_ctas(k, groups * static_cast<size_t>(nranks) * static_cast<size_t>(nranks));
-    alltoall_kernel<DT, LP, ALIGNED><<<grid, kThreads, 0, st>>>(p, nranks, c, nbc, groups);
+    const size_t pairs = static_cast<size_t>(nranks) * static_cast<size_t>(nranks);
+    if constexpr (LP) {
+        const size_t per = static_cast<size_t>(kWideItem) * A2aLp<DT>::kItems;
+        const size_t groups = (c + per - 1) / per;
+        const size_t nbc = (c + kBlock - 1) / kBlock;
+        const void *k = reinterpret_cast<const void *>(&alltoall_lp_kernel<DT, ALIGNED>);
+        const int grid = wave_ctas(k, groups * pairs, A2aLp<DT>::kCtas);
+        alltoall_lp_kernel<DT, ALIGNED><<<grid, kThreads, 0, st>>>(p, nranks, c, nbc, groups);
+    } else {
+        const size_t groups = item_groups<DT>(c);
+        const void *k = reinterpret_cast<const void *>(&alltoall_kernel<DT, ALIGNED>);
+        const int grid = wave_ctas(k, groups * pairs);
+        alltoall_kernel<DT, ALIGNED><<<grid, kThreads, 0, st>>>(p, nranks, c, groups);
+    }
     return cudaGetLastError();
 }
 

@@ -81,7 +81,7 @@ def test_all_gather(oracle, dt, block, N, m):
 @pytest.mark.parametrize("dt", [W.F32, W.BF16])
 @pytest.mark.parametrize("block", [128, 0])
 @pytest.mark.parametrize("N", [1, 2, 5, 8])
-@pytest.mark.parametrize("c", [1, 3, 130, 200, 256, 1001, 32 * 8 * 9])
+@pytest.mark.parametrize("c", [1, 3, 130, 200, 256, 1001, 32 * 8 * 9, 4096 + 8])
 def test_all_to_all(oracle, dt, block, N, c):
     ins = W.random_inputs(N, N * c, dt, 9900 + 13 * N + c, scale_spread=3.0)
     outs = [Guarded(N * c, TDT[dt]) for _ in range(N)]
