@@ -36,7 +36,11 @@
  *     n elements is codes[n] (one byte each, element order) plus
  *     scales[ceil(n / 128)] (block b covers elements [128 b, 128 b + 128)).
  *   - stream is a cudaStream_t passed as void* (NULL = legacy default
- *     stream). Work is enqueued on it and the call returns at once.
+ *     stream). Work is enqueued on it and the call returns at once. Kernels
+ *     are launched with programmatic dependent launch: one may be scheduled
+ *     while the previous kernel of the stream still runs, but it touches no
+ *     memory before that kernel has completed, so stream order holds for
+ *     every buffer, also inside CUDA graph capture.
  *   - Return value: LPCOLL_OK, or an lpcoll_status error found before any
  *     launch (nothing is enqueued then), or LPCOLL_ERR_CUDA if the launch
  *     itself failed (lpcoll_last_cuda_error() gives the cudaError_t).

@@ -45,6 +45,7 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads)
 quantize_kernel(const void *in, uint8_t *codes, float *scales, size_t n, size_t items)
 {
+    wait_prior_grid();
     constexpr int V = Fmt<DT>::kVec;
     constexpr int S = kWideElems / V;
     const int lane = threadIdx.x & 31;
@@ -76,6 +77,7 @@ __global__ void __launch_bounds__(kThreads)
 dequantize_kernel(const uint8_t *codes, const float *scales, void *out, size_t n,
                   size_t items)
 {
+    wait_prior_grid();
     constexpr int K = kDequantizeUnits;
     constexpr int V = Fmt<DT>::kVec;
     const int lane = threadIdx.x & 31;
@@ -109,6 +111,7 @@ template <int N, int DT>
 __global__ void __launch_bounds__(kThreads)
 reduce_kernel(const __grid_constant__ ReduceParams p, void *out, size_t n, size_t items)
 {
+    wait_prior_grid();
     __shared__ uint4 stage_all[kWarpsPerCta][kWideElems * 32 / 4];
     uint4 *stage = stage_all[threadIdx.x >> 5];
     const int lane = threadIdx.x & 31;
@@ -162,8 +165,7 @@ cudaError_t launch_quantize_t(const void *in, uint8_t *codes, float *scales,
     const size_t items = wide_items(n);
     const int grid = wave_ctas(reinterpret_cast<const void *>(&quantize_kernel<DT>), items,
                                kQuantizeCtasPerSm);
-    quantize_kernel<DT><<<grid, kThreads, 0, stream>>>(in, codes, scales, n, items);
-    return cudaGetLastError();
+    return launch_kernel(quantize_kernel<DT>, grid, stream, in, codes, scales, n, items);
 }
 
 template <int DT>
@@ -173,8 +175,7 @@ cudaError_t launch_dequantize_t(const uint8_t *codes, const float *scales, void 
     const size_t items = items_of<DT, kDequantizeUnits>(n);
     const int grid =
         wave_ctas(reinterpret_cast<const void *>(&dequantize_kernel<DT>), items);
-    dequantize_kernel<DT><<<grid, kThreads, 0, stream>>>(codes, scales, out, n, items);
-    return cudaGetLastError();
+    return launch_kernel(dequantize_kernel<DT>, grid, stream, codes, scales, out, n, items);
 }
 
 template <int N, int DT>
@@ -184,8 +185,7 @@ cudaError_t launch_reduce_n(const ReduceParams &p, void *out, size_t n,
     const size_t items = wide_items(n);
     const int grid =
         wave_ctas(reinterpret_cast<const void *>(&reduce_kernel<N, DT>), items);
-    reduce_kernel<N, DT><<<grid, kThreads, 0, stream>>>(p, out, n, items);
-    return cudaGetLastError();
+    return launch_kernel(reduce_kernel<N, DT>, grid, stream, p, out, n, items);
 }
 
 template <int DT>

@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(kThreads)
 dda_kernel(const __grid_constant__ DdaParams p, size_t n, size_t full_units,
            size_t total_units)
 {
+    wait_prior_grid();
     constexpr int K = units_per_iter<N>();
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
@@ -210,8 +211,7 @@ cudaError_t launch_dda_n(const DdaParams &p, size_t n, cudaStream_t stream)
     const size_t in_bytes = n * static_cast<size_t>(N) * (16 / Fmt<DT>::kVec);
     const int cap = (scatter || in_bytes < kSmallLaunchBytes) ? kCtasPerSmBusy : kCtasPerSm;
     const int grid = wave_ctas(k, (total + K - 1) / K, cap);
-    dda_kernel<N, DT, MODE><<<grid, kThreads, 0, stream>>>(p, n, full, total);
-    return cudaGetLastError();
+    return launch_kernel(dda_kernel<N, DT, MODE>, grid, stream, p, n, full, total);
 }
 
 template <int DT, int MODE>

@@ -36,6 +36,41 @@ constexpr int kCtasPerSm = 2;
 constexpr int kCtasPerSmBusy = 4;
 constexpr size_t kSmallLaunchBytes = size_t(256) << 20;
 
+// ---------------------------------------------------------------------------
+// Launch. Every kernel of the library is launched with programmatic stream
+// serialization (programmatic dependent launch), so the GPU may schedule it
+// while the previous kernel of its stream is still running; its first
+// instruction (wait_prior_grid) then waits until that kernel has completed
+// and its memory writes are visible, so the stream order of all memory
+// accesses is kept. What it saves is the gap between back-to-back launches:
+// on GB300 the 8-rank 512 KiB decode allreduce went from 2.08 to 1.63 us per
+// call in a CUDA graph and from 4.08 to 3.09 us launched back to back, with
+// chained in-place calls bit-identical. No kernel triggers its dependents
+// early (measured no faster).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void wait_prior_grid()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(Params...), int grid, cudaStream_t stream,
+                          Args... args)
+{
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // What a fused launch computes: the allreduce (exact, LP flat, LP tree) or a
 // reduce-scatter (exact or LP), whose result goes to the shard's owner only.
 enum Mode { kExact = 0, kFlat = 1, kTree = 2, kScatterExact = 3, kScatterLp = 4 };

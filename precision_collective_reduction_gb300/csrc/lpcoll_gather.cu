@@ -97,6 +97,7 @@ template <int DT, bool LP, bool ALIGNED>
 __global__ void __launch_bounds__(kThreads)
 gather_kernel(const __grid_constant__ DdaParams p, int nranks, size_t m, size_t groups)
 {
+    wait_prior_grid();
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
@@ -136,6 +137,7 @@ template <int DT, bool ALIGNED>
 __global__ void __launch_bounds__(kThreads)
 alltoall_kernel(const __grid_constant__ DdaParams p, int nranks, size_t c, size_t groups)
 {
+    wait_prior_grid();
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
@@ -213,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, A2aLp<DT>::kCtas)
 alltoall_lp_kernel(const __grid_constant__ DdaParams p, int nranks, size_t c, size_t nbc,
                    size_t groups)
 {
+    wait_prior_grid();
     __shared__ uint4 stage_all[kWarpsPerCta][kWideElems * 32 / 4];
     uint4 *stage = stage_all[threadIdx.x >> 5];
     const int lane = threadIdx.x & 31;
@@ -244,8 +247,7 @@ cudaError_t launch_gather_t(const DdaParams &p, int nranks, size_t m, cudaStream
     const size_t groups = item_groups<DT>(m);
     const void *k = reinterpret_cast<const void *>(&gather_kernel<DT, LP, ALIGNED>);
     const int grid = wave_ctas(k, groups * static_cast<size_t>(nranks));
-    gather_kernel<DT, LP, ALIGNED><<<grid, kThreads, 0, st>>>(p, nranks, m, groups);
-    return cudaGetLastError();
+    return launch_kernel(gather_kernel<DT, LP, ALIGNED>, grid, st, p, nranks, m, groups);
 }
 
 template <int DT, bool LP, bool ALIGNED>
@@ -258,14 +260,14 @@ cudaError_t launch_alltoall_t(const DdaParams &p, int nranks, size_t c, cudaStre
         const size_t nbc = (c + kBlock - 1) / kBlock;
         const void *k = reinterpret_cast<const void *>(&alltoall_lp_kernel<DT, ALIGNED>);
         const int grid = wave_ctas(k, groups * pairs, A2aLp<DT>::kCtas);
-        alltoall_lp_kernel<DT, ALIGNED><<<grid, kThreads, 0, st>>>(p, nranks, c, nbc, groups);
+        return launch_kernel(alltoall_lp_kernel<DT, ALIGNED>, grid, st, p, nranks, c, nbc,
+                             groups);
     } else {
         const size_t groups = item_groups<DT>(c);
         const void *k = reinterpret_cast<const void *>(&alltoall_kernel<DT, ALIGNED>);
         const int grid = wave_ctas(k, groups * pairs);
-        alltoall_kernel<DT, ALIGNED><<<grid, kThreads, 0, st>>>(p, nranks, c, groups);
+        return launch_kernel(alltoall_kernel<DT, ALIGNED>, grid, st, p, nranks, c, groups);
     }
-    return cudaGetLastError();
 }
 
 template <int DT>

@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kThreads)
 quantize_fmt_kernel(const void *in, uint8_t *codes, float *scales, size_t n, int block,
                     size_t groups)
 {
+    wait_prior_grid();
     constexpr int V = Fmt<DT>::kVec;
     constexpr int K = kVariantUnits;
     const int lane = threadIdx.x & 31;
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(kThreads)
 dequantize_fmt_kernel(const uint8_t *codes, const float *scales, void *out, size_t n,
                       int block, size_t groups)
 {
+    wait_prior_grid();
     constexpr int V = Fmt<DT>::kVec;
     constexpr int K = kVariantUnits;
     const int lane = threadIdx.x & 31;
@@ -194,6 +196,7 @@ __global__ void __launch_bounds__(kThreads)
 reduce_fmt_kernel(const __grid_constant__ ReduceParams p, int nranks, void *out, size_t n,
                   int block, size_t units)
 {
+    wait_prior_grid();
     constexpr int V = Fmt<DT>::kVec;
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
@@ -225,14 +228,12 @@ cudaError_t quantize_fmt_t(const void *in, size_t n, int block, uint8_t *codes,
     const size_t groups = (units + kVariantUnits - 1) / kVariantUnits;
     if (block > 32 * Fmt<DT>::kVec) {  // FP32, block 256: two units per block
         const void *k = reinterpret_cast<const void *>(&quantize_fmt_kernel<DT, FMT, 2>);
-        quantize_fmt_kernel<DT, FMT, 2>
-            <<<wave_ctas(k, groups), kThreads, 0, st>>>(in, codes, scales, n, block, groups);
-    } else {
-        const void *k = reinterpret_cast<const void *>(&quantize_fmt_kernel<DT, FMT, 1>);
-        quantize_fmt_kernel<DT, FMT, 1>
-            <<<wave_ctas(k, groups), kThreads, 0, st>>>(in, codes, scales, n, block, groups);
+        return launch_kernel(quantize_fmt_kernel<DT, FMT, 2>, wave_ctas(k, groups), st, in,
+                             codes, scales, n, block, groups);
     }
-    return cudaGetLastError();
+    const void *k = reinterpret_cast<const void *>(&quantize_fmt_kernel<DT, FMT, 1>);
+    return launch_kernel(quantize_fmt_kernel<DT, FMT, 1>, wave_ctas(k, groups), st, in, codes,
+                         scales, n, block, groups);
 }
 
 template <int DT, int FMT>
@@ -243,9 +244,8 @@ cudaError_t dequantize_fmt_t(const uint8_t *codes, const float *scales, size_t n
     unit_counts<DT>(n, full, units);
     const size_t groups = (units + kVariantUnits - 1) / kVariantUnits;
     const void *k = reinterpret_cast<const void *>(&dequantize_fmt_kernel<DT, FMT>);
-    dequantize_fmt_kernel<DT, FMT>
-        <<<wave_ctas(k, groups), kThreads, 0, st>>>(codes, scales, out, n, block, groups);
-    return cudaGetLastError();
+    return launch_kernel(dequantize_fmt_kernel<DT, FMT>, wave_ctas(k, groups), st, codes,
+                         scales, out, n, block, groups);
 }
 
 template <int DT, int FMT>
@@ -255,9 +255,8 @@ cudaError_t reduce_fmt_t(const ReduceParams &p, int nranks, size_t n, int block,
     size_t full, units;
     unit_counts<DT>(n, full, units);
     const void *k = reinterpret_cast<const void *>(&reduce_fmt_kernel<DT, FMT>);
-    reduce_fmt_kernel<DT, FMT>
-        <<<wave_ctas(k, units), kThreads, 0, st>>>(p, nranks, out, n, block, units);
-    return cudaGetLastError();
+    return launch_kernel(reduce_fmt_kernel<DT, FMT>, wave_ctas(k, units), st, p, nranks, out, n,
+                         block, units);
 }
 
 #define LPC_BY_TYPE(FN, DTYPE, FMT, ...)                                              \

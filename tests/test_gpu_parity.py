@@ -297,6 +297,64 @@ def test_cuda_graph_replay(oracle, block):
         assert_same(from_dev(outs[r]), want[r], "out[%d]" % r)
 
 
+@pytest.mark.parametrize("graph", [False, True])
+def test_chained_launches_keep_stream_order(oracle, graph):
+    """Back-to-back dependent calls on one stream with no synchronisation in
+    between, each reading what the previous one wrote: in-place flat and tree
+    allreduces (exact and low precision), then a staged quantize -> reduce.
+    The kernels are launched with programmatic dependent launch; the result
+    must be the oracle's chain of the same calls, eagerly and replayed from a
+    CUDA graph."""
+    N, n = 8, 32 * 8192 + 77
+    ins = W.random_inputs(N, n, BF16, 8300, scale_spread=1.0)
+    chain = [("flat", 0), ("flat", 128), ("tree", 128), ("flat", 128), ("tree", 0),
+             ("flat", 128)]
+    want = [x.copy() for x in ins]
+    for algo, block in chain:
+        res = (oracle.flat if algo == "flat" else oracle.tree)(want, block=block)[0]
+        want = [r.copy() for r in res]
+    pays = [oracle.quantize(x) for x in want]
+    want_red = oracle.reduce([c for c, _ in pays], [s for _, s in pays], dtype=np.uint16)
+
+    xd = [to_dev(x) for x in ins]
+    wc = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(N)]
+    ws = [torch.empty(pcr.nblocks(n), dtype=torch.float32, device="cuda") for _ in range(N)]
+    sc = torch.empty(n, dtype=torch.uint8, device="cuda")
+    ss = torch.empty(pcr.nblocks(n), dtype=torch.float32, device="cuda")
+    red = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+
+    def calls():
+        for algo, block in chain:
+            kw = dict(wire_codes=wc, wire_scales=ws) if block else {}
+            if algo == "flat":
+                pcr.dda_flat_sim(xd, xd, block=block, stream=s, **kw)
+            else:
+                if block:
+                    kw.update(shard_codes=sc, shard_scales=ss)
+                pcr.dda_tree_sim(xd, xd, block=block, stream=s, **kw)
+        for r in range(N):
+            pcr.lp_quantize(xd[r], wc[r], ws[r], stream=s)
+        pcr.lp_reduce(wc, ws, red, stream=s)
+
+    torch.cuda.synchronize()
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            calls()
+        for t, x in zip(xd, ins):   # capture ran nothing; start from the inputs
+            t.copy_(to_dev(x))
+        torch.cuda.synchronize()
+        g.replay()
+    else:
+        with torch.cuda.stream(s):
+            calls()
+    torch.cuda.synchronize()
+    for r in range(N):
+        assert_same(from_dev(xd[r]), want[r], "chained out[%d]" % r)
+    assert_same(from_dev(red), want_red, "chained reduce")
+
+
 def test_pages_example_with_host_tensors():
     # the example as the pages write it: torch.full on the host, SUM in place
     from oracle_pins import read_torch_full_cases
