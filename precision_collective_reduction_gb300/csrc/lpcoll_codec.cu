@@ -41,7 +41,9 @@ __device__ __forceinline__ void unit_lanes(size_t n, size_t u0, int lane, size_t
     }
 }
 
-template <int DT>
+// FP8 format FMT on blocks of G lanes (16 G elements): the main path is
+// <DT, E4M3, 8>, the format / block-size variants the other instances.
+template <int DT, int FMT, int G>
 __global__ void __launch_bounds__(kThreads)
 quantize_kernel(const void *in, uint8_t *codes, float *scales, size_t n, size_t items)
 {
@@ -63,11 +65,11 @@ quantize_kernel(const void *in, uint8_t *codes, float *scales, size_t n, size_t 
         wide_widen<DT>(raw, x);
         float s;
         uint32_t w[4];
-        wide_quantize(x, w, s);
+        wide_quantize_fmt<FMT, G>(x, w, s);
         if (e0 < n) {
             wide_store_codes(codes, n, e0, w);
-            if (lane % kWideGroup == 0)
-                __stcs(scales + e0 / kBlock, s);
+            if (lane % G == 0)
+                __stcs(scales + e0 / (kWideElems * G), s);
         }
     }
 }
@@ -158,14 +160,29 @@ inline size_t items_of(size_t n)
 // Warp items of the wide layout covering a message of n elements.
 inline size_t wide_items(size_t n) { return (n + kWideItem - 1) / kWideItem; }
 
-template <int DT>
-cudaError_t launch_quantize_t(const void *in, uint8_t *codes, float *scales,
-                              size_t n, cudaStream_t stream)
+template <int DT, int FMT, int G>
+cudaError_t launch_quantize_t(const void *in, uint8_t *codes, float *scales, size_t n,
+                              cudaStream_t stream)
 {
     const size_t items = wide_items(n);
-    const int grid = wave_ctas(reinterpret_cast<const void *>(&quantize_kernel<DT>), items,
-                               kQuantizeCtasPerSm);
-    return launch_kernel(quantize_kernel<DT>, grid, stream, in, codes, scales, n, items);
+    const int grid = wave_ctas(reinterpret_cast<const void *>(&quantize_kernel<DT, FMT, G>),
+                               items, kQuantizeCtasPerSm);
+    return launch_kernel(quantize_kernel<DT, FMT, G>, grid, stream, in, codes, scales, n,
+                         items);
+}
+
+// Block size (32, 64, 128 or 256 elements) -> lanes per block.
+template <int DT, int FMT>
+cudaError_t launch_quantize_blocks(const void *in, size_t n, int block, uint8_t *codes,
+                                   float *scales, cudaStream_t stream)
+{
+    switch (block) {
+    case 32: return launch_quantize_t<DT, FMT, 2>(in, codes, scales, n, stream);
+    case 64: return launch_quantize_t<DT, FMT, 4>(in, codes, scales, n, stream);
+    case 128: return launch_quantize_t<DT, FMT, 8>(in, codes, scales, n, stream);
+    case 256: return launch_quantize_t<DT, FMT, 16>(in, codes, scales, n, stream);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 template <int DT>
@@ -207,8 +224,26 @@ cudaError_t launch_quantize(const void *in, int dtype, size_t n, uint8_t *codes,
                             float *scales, cudaStream_t stream)
 {
     return dtype == LPCOLL_F32
-               ? launch_quantize_t<LPCOLL_F32>(in, codes, scales, n, stream)
-               : launch_quantize_t<LPCOLL_BF16>(in, codes, scales, n, stream);
+               ? launch_quantize_t<LPCOLL_F32, LPCOLL_E4M3, kWideGroup>(in, codes, scales, n,
+                                                                        stream)
+               : launch_quantize_t<LPCOLL_BF16, LPCOLL_E4M3, kWideGroup>(in, codes, scales, n,
+                                                                         stream);
+}
+
+cudaError_t launch_quantize_fmt(const void *in, int dtype, size_t n, int block, int fmt,
+                                uint8_t *codes, float *scales, cudaStream_t stream)
+{
+    if (dtype == LPCOLL_F32)
+        return fmt == LPCOLL_E4M3
+                   ? launch_quantize_blocks<LPCOLL_F32, LPCOLL_E4M3>(in, n, block, codes,
+                                                                    scales, stream)
+                   : launch_quantize_blocks<LPCOLL_F32, LPCOLL_E5M2>(in, n, block, codes,
+                                                                    scales, stream);
+    return fmt == LPCOLL_E4M3
+               ? launch_quantize_blocks<LPCOLL_BF16, LPCOLL_E4M3>(in, n, block, codes, scales,
+                                                                 stream)
+               : launch_quantize_blocks<LPCOLL_BF16, LPCOLL_E5M2>(in, n, block, codes, scales,
+                                                                 stream);
 }
 
 cudaError_t launch_dequantize(const uint8_t *codes, const float *scales, size_t n,

@@ -1,5 +1,6 @@
 // lpcoll_variants.cu -- format and block-size variants of the staged building
-// blocks: lp_quantize_fmt, lp_dequantize_fmt, lp_reduce_fmt.
+// blocks: lp_dequantize_fmt and lp_reduce_fmt (lp_quantize_fmt is the
+// quantize kernel of lpcoll_codec.cu, instantiated per format and block).
 //
 // The pages fix neither the FP8 format nor the scaling granularity; these
 // entry points make both a parameter for ablations: OCP E4M3 (largest finite
@@ -9,64 +10,17 @@
 // fl(fp8 * s), FP32 sums in rank order. With E4M3 and 128-element blocks the
 // results equal lp_quantize / lp_dequantize / lp_reduce.
 //
-// Work decomposition: a warp-unit is 32 lanes x 16 bytes (kVec elements per
-// lane), so a block spans block / kVec lanes; FP32 blocks of 256 span two
-// units, which one warp then processes together (U = 2). A warp takes 4
-// consecutive units per iteration, all loads first.
+// Dequantize works on warp-units (32 lanes x 16 bytes, 4 units per warp
+// iteration, all loads first). The reduce works on the wide lane layout (16
+// elements per lane, so no lane's elements straddle a block of 32 or more)
+// and, the rank count being a run-time value, issues the loads of 4 ranks at
+// a time before it adds them in rank order; results go out through the
+// warp's shared-memory stage.
 #include "lpcoll_dda.cuh"
 #include "lpcoll_device.cuh"
+#include "lpcoll_wide.cuh"
 
 namespace lpc {
-
-template <int FMT> struct Fp8;
-template <> struct Fp8<LPCOLL_E4M3> {
-    static constexpr float kMax = 448.0f;
-    static constexpr __nv_fp8_interpretation_t kKind = __NV_E4M3;
-};
-template <> struct Fp8<LPCOLL_E5M2> {
-    static constexpr float kMax = 57344.0f;
-    static constexpr __nv_fp8_interpretation_t kKind = __NV_E5M2;
-};
-
-// Largest |x| over groups of G lanes (G a power of two <= 32, uniform).
-__device__ __forceinline__ float group_max_rt(float v, int G)
-{
-    for (int m = G >> 1; m >= 1; m >>= 1)
-        v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
-    return v;
-}
-
-template <int FMT>
-__device__ __forceinline__ void block_scale_fmt(float amax, float &s, float &inv)
-{
-    inv = __fdiv_rn(Fp8<FMT>::kMax, amax);
-    if (isinf(inv)) {
-        inv = 0.0f;
-        s = 0.0f;
-    } else {
-        s = __fdiv_rn(amax, Fp8<FMT>::kMax);
-    }
-}
-
-// kVec values -> packed codes (element 0 in the low byte).
-template <int DT, int FMT>
-__device__ __forceinline__ Codes<DT> encode_lane(const float (&x)[Fmt<DT>::kVec],
-                                                 float inv)
-{
-    constexpr int V = Fmt<DT>::kVec;
-    uint32_t c2[V / 2];
-#pragma unroll
-    for (int j = 0; j < V / 2; ++j)
-        c2[j] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
-            make_float2(__fmul_rn(x[2 * j], inv), __fmul_rn(x[2 * j + 1], inv)),
-            __NV_SATFINITE, Fp8<FMT>::kKind));
-    Codes<DT> c;
-    if constexpr (DT == LPCOLL_F32)
-        c.w = c2[0] | (c2[1] << 16);
-    else
-        c.w = make_uint2(c2[0] | (c2[1] << 16), c2[2] | (c2[3] << 16));
-    return c;
-}
 
 template <int FMT>
 __device__ __forceinline__ float2 dec2_fmt(uint32_t c2)
@@ -99,61 +53,11 @@ __device__ __forceinline__ void decode_lane(Codes<DT> c, float s,
     }
 }
 
-// Units per loop iteration of the quantize / dequantize variants; all their
-// loads are issued before any unit is processed (as in lp_quantize).
+// Units per loop iteration of the dequantize variant; all their loads are
+// issued before any unit is processed (as in lp_dequantize).
 constexpr int kVariantUnits = 4;
-
-// Quantize kVariantUnits consecutive units per iteration. A block covers G
-// lanes of one unit (U = 1) or the whole of two units (U = 2: FP32 blocks of
-// 256 elements); U divides kVariantUnits, so no block straddles iterations.
-template <int DT, int FMT, int U>
-__global__ void __launch_bounds__(kThreads)
-quantize_fmt_kernel(const void *in, uint8_t *codes, float *scales, size_t n, int block,
-                    size_t groups)
-{
-    wait_prior_grid();
-    constexpr int V = Fmt<DT>::kVec;
-    constexpr int K = kVariantUnits;
-    const int lane = threadIdx.x & 31;
-    const int G = (U == 2) ? 32 : block / V;
-    const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-    const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
-    for (size_t g = warp; g < groups; g += nwarps) {
-        size_t e0[K];
-        int cnt[K];
-        uint4 raw[K];
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-            e0[k] = ((g * K + k) * 32 + lane) * V;
-            cnt[k] = lane_count<DT>(n, e0[k]);
-            raw[k] = cnt[k] > 0 ? load_vec<DT>(in, e0[k], cnt[k]) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int i = 0; i < K; i += U) {
-            float x[U][V];
-            float amax = 0.0f;
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                widen<DT>(raw[i + k], x[k]);
-                float a = 0.0f;
-#pragma unroll
-                for (int j = 0; j < V; ++j)
-                    a = fmaxf(a, fabsf(x[k][j]));
-                amax = fmaxf(amax, group_max_rt(a, G));
-            }
-            float s, inv;
-            block_scale_fmt<FMT>(amax, s, inv);
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                if (cnt[i + k] > 0) {
-                    store_codes(codes, e0[i + k], cnt[i + k], encode_lane<DT, FMT>(x[k], inv));
-                    if (k == 0 && (lane % G) == 0)
-                        scales[e0[i] / block] = s;
-                }
-            }
-        }
-    }
-}
+// Ranks whose loads the reduce variant issues together.
+constexpr int kRankChunk = 4;
 
 template <int DT, int FMT>
 __global__ void __launch_bounds__(kThreads)
@@ -194,46 +98,47 @@ dequantize_fmt_kernel(const uint8_t *codes, const float *scales, void *out, size
 template <int DT, int FMT>
 __global__ void __launch_bounds__(kThreads)
 reduce_fmt_kernel(const __grid_constant__ ReduceParams p, int nranks, void *out, size_t n,
-                  int block, size_t units)
+                  int block_shift, size_t items)
 {
     wait_prior_grid();
-    constexpr int V = Fmt<DT>::kVec;
+    __shared__ uint4 stage_all[kWarpsPerCta][kWideElems * 32 / 4];
+    uint4 *stage = stage_all[threadIdx.x >> 5];
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
-    for (size_t u = warp; u < units; u += nwarps) {
-        const size_t e0 = (u * 32 + lane) * V;
-        const int cnt = lane_count<DT>(n, e0);
-        if (cnt <= 0)
-            continue;
-        float acc[V];
-        for (int r = 0; r < nranks; ++r) {
-            float v[V];
-            decode_lane<DT, FMT>(load_codes<DT>(p.codes[r], e0, cnt),
-                                 p.scales[r][e0 / block], v);
+    for (size_t it = warp; it < items; it += nwarps) {
+        const size_t item_e0 = it * kWideItem;
+        const size_t e0 = item_e0 + static_cast<size_t>(lane) * kWideElems;
+        float acc[kWideElems];
 #pragma unroll
-            for (int j = 0; j < V; ++j)
-                acc[j] = (r == 0) ? v[j] : __fadd_rn(acc[j], v[j]);
+        for (int j = 0; j < kWideElems; ++j)
+            acc[j] = 0.0f;
+        if (e0 < n) {
+            const size_t b = e0 >> block_shift;
+            for (int r0 = 0; r0 < nranks; r0 += kRankChunk) {
+                uint4 c[kRankChunk];
+                float s[kRankChunk];
+#pragma unroll
+                for (int k = 0; k < kRankChunk; ++k) {
+                    if (r0 + k < nranks) {
+                        c[k] = wide_load_codes(p.codes[r0 + k], n, e0);
+                        s[k] = p.scales[r0 + k][b];
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kRankChunk; ++k) {
+                    if (r0 + k < nranks) {
+                        float v[kWideElems];
+                        wide_dequant_fmt<FMT>(c[k], s[k], v);
+#pragma unroll
+                        for (int j = 0; j < kWideElems; ++j)
+                            acc[j] = (r0 + k == 0) ? v[j] : __fadd_rn(acc[j], v[j]);
+                    }
+                }
+            }
         }
-        store_vec<DT>(out, e0, cnt, narrow<DT>(acc));
+        wide_store_results<DT>(out, n, item_e0, acc, stage, lane);
     }
-}
-
-template <int DT, int FMT>
-cudaError_t quantize_fmt_t(const void *in, size_t n, int block, uint8_t *codes,
-                           float *scales, cudaStream_t st)
-{
-    size_t full, units;
-    unit_counts<DT>(n, full, units);
-    const size_t groups = (units + kVariantUnits - 1) / kVariantUnits;
-    if (block > 32 * Fmt<DT>::kVec) {  // FP32, block 256: two units per block
-        const void *k = reinterpret_cast<const void *>(&quantize_fmt_kernel<DT, FMT, 2>);
-        return launch_kernel(quantize_fmt_kernel<DT, FMT, 2>, wave_ctas(k, groups), st, in,
-                             codes, scales, n, block, groups);
-    }
-    const void *k = reinterpret_cast<const void *>(&quantize_fmt_kernel<DT, FMT, 1>);
-    return launch_kernel(quantize_fmt_kernel<DT, FMT, 1>, wave_ctas(k, groups), st, in, codes,
-                         scales, n, block, groups);
 }
 
 template <int DT, int FMT>
@@ -252,11 +157,13 @@ template <int DT, int FMT>
 cudaError_t reduce_fmt_t(const ReduceParams &p, int nranks, size_t n, int block,
                          void *out, cudaStream_t st)
 {
-    size_t full, units;
-    unit_counts<DT>(n, full, units);
+    const size_t items = (n + kWideItem - 1) / kWideItem;
+    int shift = 0;
+    while ((1 << shift) < block)
+        ++shift;
     const void *k = reinterpret_cast<const void *>(&reduce_fmt_kernel<DT, FMT>);
-    return launch_kernel(reduce_fmt_kernel<DT, FMT>, wave_ctas(k, units), st, p, nranks, out, n,
-                         block, units);
+    return launch_kernel(reduce_fmt_kernel<DT, FMT>, wave_ctas(k, items), st, p, nranks, out, n,
+                         shift, items);
 }
 
 #define LPC_BY_TYPE(FN, DTYPE, FMT, ...)                                              \
@@ -265,12 +172,6 @@ cudaError_t reduce_fmt_t(const ReduceParams &p, int nranks, size_t n, int block,
                                  : FN<LPCOLL_F32, LPCOLL_E5M2>(__VA_ARGS__))         \
          : ((FMT) == LPCOLL_E4M3 ? FN<LPCOLL_BF16, LPCOLL_E4M3>(__VA_ARGS__)         \
                                  : FN<LPCOLL_BF16, LPCOLL_E5M2>(__VA_ARGS__)))
-
-cudaError_t launch_quantize_fmt(const void *in, int dtype, size_t n, int block, int fmt,
-                                uint8_t *codes, float *scales, cudaStream_t st)
-{
-    return LPC_BY_TYPE(quantize_fmt_t, dtype, fmt, in, n, block, codes, scales, st);
-}
 
 cudaError_t launch_dequantize_fmt(const uint8_t *codes, const float *scales, size_t n,
                                   int block, int fmt, void *out, int dtype, cudaStream_t st)

@@ -48,19 +48,42 @@ __device__ __forceinline__ void wide_store_codes(uint8_t *codes, size_t n, size_
             codes[e0 + j] = static_cast<uint8_t>(w[j / 4] >> (8 * (j % 4)));
 }
 
-// v = fl(e4m3(code) * s) for the 16 codes of a wide lane.
-__device__ __forceinline__ void wide_dequant(uint4 c, float s, float (&v)[kWideElems])
+// OCP FP8 formats: largest finite value and the conversion's interpretation.
+template <int FMT> struct Fp8;
+template <> struct Fp8<LPCOLL_E4M3> {
+    static constexpr float kMax = 448.0f;
+    static constexpr __nv_fp8_interpretation_t kKind = __NV_E4M3;
+};
+template <> struct Fp8<LPCOLL_E5M2> {
+    static constexpr float kMax = 57344.0f;
+    static constexpr __nv_fp8_interpretation_t kKind = __NV_E5M2;
+};
+
+// v = fl(fp8(code) * s) for the 16 codes of a wide lane (the FP8 -> FP16
+// conversion is exact for both formats).
+template <int FMT>
+__device__ __forceinline__ void wide_dequant_fmt(uint4 c, float s, float (&v)[kWideElems])
 {
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const float2 lo = dec2(w[q]);
-        const float2 hi = dec2(w[q] >> 16);
+        const __half2_raw lo_h = __nv_cvt_fp8x2_to_halfraw2(
+            static_cast<__nv_fp8x2_storage_t>(w[q] & 0xFFFFu), Fp8<FMT>::kKind);
+        const __half2_raw hi_h = __nv_cvt_fp8x2_to_halfraw2(
+            static_cast<__nv_fp8x2_storage_t>(w[q] >> 16), Fp8<FMT>::kKind);
+        const float2 lo = __half22float2(__half2(lo_h));
+        const float2 hi = __half22float2(__half2(hi_h));
         v[4 * q + 0] = __fmul_rn(lo.x, s);
         v[4 * q + 1] = __fmul_rn(lo.y, s);
         v[4 * q + 2] = __fmul_rn(hi.x, s);
         v[4 * q + 3] = __fmul_rn(hi.y, s);
     }
+}
+
+// The main path's E4M3 decoding.
+__device__ __forceinline__ void wide_dequant(uint4 c, float s, float (&v)[kWideElems])
+{
+    wide_dequant_fmt<LPCOLL_E4M3>(c, s, v);
 }
 
 // Store the 16 results of every lane of a warp item (first element item_e0)
@@ -101,22 +124,44 @@ __device__ __forceinline__ void wide_store_results(void *out, size_t n, size_t i
     __syncwarp();
 }
 
-// Quantize the 16 values of a wide lane on its block (8-lane group): the
-// packed codes (element 4q + i in byte i of w[q]) and the block scale s.
-__device__ __forceinline__ void wide_quantize(const float (&x)[kWideElems], uint32_t (&w)[4],
-                                              float &s)
+// Quantize the 16 values of a wide lane on its block of G lanes (16 G
+// elements): a = block max |x|, s = fl(a / max), codes = fp8(fl(x * fl(max /
+// a))) rounded to nearest even and saturated; a block whose max / a
+// overflows gets s = 0 and signed-zero codes. Packed codes: element 4q + i
+// in byte i of w[q].
+template <int FMT, int G>
+__device__ __forceinline__ void wide_quantize_fmt(const float (&x)[kWideElems], uint32_t (&w)[4],
+                                                  float &s)
 {
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < kWideElems; ++i)
         amax = fmaxf(amax, fabsf(x[i]));
-    amax = group_max<kWideGroup>(amax);
-    float inv;
-    block_scale(amax, s, inv);
+    amax = group_max<G>(amax);
+    float inv = __fdiv_rn(Fp8<FMT>::kMax, amax);
+    if (isinf(inv)) {
+        inv = 0.0f;
+        s = 0.0f;
+    } else {
+        s = __fdiv_rn(amax, Fp8<FMT>::kMax);
+    }
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-        w[q] = enc2(__fmul_rn(x[4 * q], inv), __fmul_rn(x[4 * q + 1], inv)) |
-               (enc2(__fmul_rn(x[4 * q + 2], inv), __fmul_rn(x[4 * q + 3], inv)) << 16);
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fmul_rn(x[4 * q], inv), __fmul_rn(x[4 * q + 1], inv)), __NV_SATFINITE,
+            Fp8<FMT>::kKind);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fmul_rn(x[4 * q + 2], inv), __fmul_rn(x[4 * q + 3], inv)),
+            __NV_SATFINITE, Fp8<FMT>::kKind);
+        w[q] = lo | (hi << 16);
+    }
+}
+
+// The main path: E4M3 on 128-element blocks.
+__device__ __forceinline__ void wide_quantize(const float (&x)[kWideElems], uint32_t (&w)[4],
+                                              float &s)
+{
+    wide_quantize_fmt<LPCOLL_E4M3, kWideGroup>(x, w, s);
 }
 
 // The values of the S = 16 / kVec vectors of a wide lane.

@@ -52,7 +52,7 @@ def test_quantize_dequantize(oracle, fmt, block, dt, n):
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("block", pcr.VARIANT_BLOCKS)
 @pytest.mark.parametrize("dt", [W.F32, W.BF16])
-@pytest.mark.parametrize("N", [1, 3, 8])
+@pytest.mark.parametrize("N", [1, 3, 5, 8, 16])
 def test_reduce(oracle, fmt, block, dt, N):
     n = 128 * 30 + 17
     ins = W.random_inputs(N, n, dt, 13000 + block + N + 5 * fmt, scale_spread=3.0)
