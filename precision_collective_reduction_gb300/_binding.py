@@ -86,6 +86,16 @@ def ptr_array(ptrs):
     return (ctypes.c_void_p * max(len(ptrs), 1))(*ptrs)
 
 
+def _rank_ptrs(ptrs, nranks, what, needed=True):
+    """ptr_array of a per-rank argument, which the C call reads nranks
+    entries of; an argument the call does not read (the wires of an exact
+    call) may be shorter."""
+    ptrs = list(ptrs) if ptrs is not None else []
+    if needed and len(ptrs) < nranks:
+        raise ValueError("%s lists %d pointers for %d ranks" % (what, len(ptrs), nranks))
+    return ptr_array(ptrs)
+
+
 def _check(st, what):
     if st != 0:
         raise LpcollError(st, what)
@@ -104,35 +114,43 @@ def raw_lp_dequantize(codes_ptr, scales_ptr, n, block, out_ptr, dtype, stream):
 
 
 def raw_lp_reduce(codes_ptrs, scales_ptrs, nranks, n, block, out_ptr, dtype, stream):
-    _check(lib().lp_reduce(ptr_array(codes_ptrs), ptr_array(scales_ptrs), nranks, n,
-                           block, out_ptr, dtype, stream), "lp_reduce")
+    _check(lib().lp_reduce(_rank_ptrs(codes_ptrs, nranks, "codes"),
+                           _rank_ptrs(scales_ptrs, nranks, "scales"), nranks, n, block,
+                           out_ptr, dtype, stream), "lp_reduce")
 
 
 def raw_dda_flat_sim(in_ptrs, out_ptrs, nranks, n, dtype, block, wc_ptrs, ws_ptrs,
                      stream):
-    _check(lib().dda_flat_sim(ptr_array(in_ptrs), ptr_array(out_ptrs), nranks, n,
-                              dtype, block, ptr_array(wc_ptrs), ptr_array(ws_ptrs),
+    _check(lib().dda_flat_sim(_rank_ptrs(in_ptrs, nranks, "in"),
+                              _rank_ptrs(out_ptrs, nranks, "out"), nranks, n, dtype, block,
+                              _rank_ptrs(wc_ptrs, nranks, "wire_codes", block != 0),
+                              _rank_ptrs(ws_ptrs, nranks, "wire_scales", block != 0),
                               stream), "dda_flat_sim")
 
 
 def raw_dda_tree_sim(in_ptrs, out_ptrs, nranks, n, dtype, block, wc_ptrs, ws_ptrs,
                      sc_ptr, ss_ptr, stream):
-    _check(lib().dda_tree_sim(ptr_array(in_ptrs), ptr_array(out_ptrs), nranks, n,
-                              dtype, block, ptr_array(wc_ptrs), ptr_array(ws_ptrs),
+    _check(lib().dda_tree_sim(_rank_ptrs(in_ptrs, nranks, "in"),
+                              _rank_ptrs(out_ptrs, nranks, "out"), nranks, n, dtype, block,
+                              _rank_ptrs(wc_ptrs, nranks, "wire_codes", block != 0),
+                              _rank_ptrs(ws_ptrs, nranks, "wire_scales", block != 0),
                               sc_ptr, ss_ptr, stream), "dda_tree_sim")
 
 
 def raw_collective(name, in_ptrs, out_ptrs, nranks, count, dtype, block, wc_ptrs,
                    ws_ptrs, stream):
     """reduce_scatter_sim / all_gather_sim / all_to_all_sim by name."""
-    _check(getattr(lib(), name)(ptr_array(in_ptrs), ptr_array(out_ptrs), nranks, count,
-                                dtype, block, ptr_array(wc_ptrs), ptr_array(ws_ptrs),
+    _check(getattr(lib(), name)(_rank_ptrs(in_ptrs, nranks, "in"),
+                                _rank_ptrs(out_ptrs, nranks, "out"), nranks, count, dtype,
+                                block, _rank_ptrs(wc_ptrs, nranks, "wire_codes", block != 0),
+                                _rank_ptrs(ws_ptrs, nranks, "wire_scales", block != 0),
                                 stream), name)
 
 
 def raw_dda_flat_sim_noalloc(in_ptrs, out_ptrs, nranks, n, dtype, stream):
-    _check(lib().dda_flat_sim_noalloc(ptr_array(in_ptrs), ptr_array(out_ptrs), nranks,
-                                      n, dtype, stream), "dda_flat_sim_noalloc")
+    _check(lib().dda_flat_sim_noalloc(_rank_ptrs(in_ptrs, nranks, "in"),
+                                      _rank_ptrs(out_ptrs, nranks, "out"), nranks, n, dtype,
+                                      stream), "dda_flat_sim_noalloc")
 
 
 # -- torch-tensor calls -----------------------------------------------------
@@ -169,6 +187,11 @@ def _need(t, what, dtype=None, numel=None):
         raise TypeError("%s must be a torch.Tensor" % what)
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % what)
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on the current device: a tensor of another
+        # GPU would be dereferenced there
+        raise ValueError("%s is on %s but the current CUDA device is cuda:%d"
+                         % (what, t.device, torch.cuda.current_device()))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % what)
     if dtype is not None and t.dtype != dtype:
@@ -216,8 +239,7 @@ def lp_reduce(codes, scales, out, block=BLOCK, stream=None):
 
 def _rank_args(ins, outs, wire_codes, wire_scales, block):
     torch = _torch()
-    if len(ins) != len(outs):
-        raise ValueError("one output per input rank")
+    _one_per_rank(ins, outs)
     n = ins[0].numel()
     dt = ins[0].dtype
     ip = [_need(t, "in[%d]" % r, dt, None) for r, t in enumerate(ins)]
@@ -282,6 +304,15 @@ def _wire_args(ins, wire_codes, wire_scales, block, ncodes, nscales):
     return wc, ws
 
 
+def _one_per_rank(ins, outs):
+    # the C call reads exactly N entries of every per-rank array
+    if len(ins) == 0:
+        raise ValueError("need at least one rank")
+    if len(outs) != len(ins):
+        raise ValueError("one output per input rank (%d inputs, %d outputs)"
+                         % (len(ins), len(outs)))
+
+
 def _inputs(ins, count):
     dt = ins[0].dtype
     ip = [_need(t, "in[%d]" % r, dt, None) for r, t in enumerate(ins)]
@@ -294,6 +325,7 @@ def reduce_scatter_sim(ins, outs, block=BLOCK, wire_codes=None, wire_scales=None
                        stream=None):
     """ReduceScatter: outs[r] (shard_len elements, the last rank's fewer; may
     be None for an empty shard) receives shard r of the sum of ``ins``."""
+    _one_per_rank(ins, outs)
     N = len(ins)
     n = ins[0].numel()
     ip, dt = _inputs(ins, n)
@@ -311,6 +343,7 @@ def reduce_scatter_sim(ins, outs, block=BLOCK, wire_codes=None, wire_scales=None
 def all_gather_sim(ins, outs, block=BLOCK, wire_codes=None, wire_scales=None,
                    stream=None):
     """AllGather: every outs[r] (N*m elements) receives all N contributions."""
+    _one_per_rank(ins, outs)
     N = len(ins)
     m = ins[0].numel()
     ip, dt = _inputs(ins, m)
@@ -325,6 +358,7 @@ def all_to_all_sim(ins, outs, block=BLOCK, wire_codes=None, wire_scales=None,
                    stream=None):
     """AlltoAll: ins[r] is N chunks of c elements; outs[j][r*c:(r+1)*c] receives
     chunk j of rank r."""
+    _one_per_rank(ins, outs)
     N = len(ins)
     total = ins[0].numel()
     if total % N:
@@ -341,6 +375,7 @@ def all_to_all_sim(ins, outs, block=BLOCK, wire_codes=None, wire_scales=None,
 def dda_flat_sim_noalloc(ins, outs, stream=None):
     """dda_flat_sim with block=128 whose wires live in the library's own
     fixed device array (for callers that cannot allocate device memory)."""
+    _one_per_rank(ins, outs)
     n = ins[0].numel()
     ip, dt = _inputs(ins, n)
     op = [_need(t, "out[%d]" % r, dt, n) for r, t in enumerate(outs)]
@@ -381,7 +416,8 @@ def lp_reduce_fmt(codes, scales, out, block, fmt, stream=None):
            for r, s in enumerate(scales)]
     if len(cps) != len(sps):
         raise ValueError("codes and scales must list the same ranks")
-    _check(lib().lp_reduce_fmt(ptr_array(cps), ptr_array(sps), len(cps), n, block, fmt,
+    _check(lib().lp_reduce_fmt(_rank_ptrs(cps, len(cps), "codes"),
+                               _rank_ptrs(sps, len(cps), "scales"), len(cps), n, block, fmt,
                                op, dtype_code(out), _stream(stream)), "lp_reduce_fmt")
     return out
 
@@ -397,9 +433,11 @@ def raw_host_allreduce(in_ptrs, flat_ptrs, tree_ptrs, nranks, n, dtype, block, c
     """lpcoll_host_allreduce with host pointers as ints; flat_ptrs / tree_ptrs
     None to skip that allreduce."""
     _check(lib().lpcoll_host_allreduce(
-        ptr_array(in_ptrs), ptr_array(flat_ptrs) if flat_ptrs is not None else None,
-        ptr_array(tree_ptrs) if tree_ptrs is not None else None, nranks, n, dtype, block,
-        chunk, slots, ws_ptr, ws_bytes, s_in, s_cmp, s_out), "lpcoll_host_allreduce")
+        _rank_ptrs(in_ptrs, nranks, "host_in"),
+        _rank_ptrs(flat_ptrs, nranks, "host_out_flat") if flat_ptrs is not None else None,
+        _rank_ptrs(tree_ptrs, nranks, "host_out_tree") if tree_ptrs is not None else None,
+        nranks, n, dtype, block, chunk, slots, ws_ptr, ws_bytes, s_in, s_cmp, s_out),
+        "lpcoll_host_allreduce")
 
 
 def _host(t, what, dtype, numel):
@@ -423,6 +461,9 @@ def lpcoll_host_allreduce(host_ins, host_out_flat=None, host_out_tree=None, bloc
     tensor of at least lpcoll_host_workspace_bytes(...) bytes; streams: three
     CUDA streams (copy in, compute, copy out)."""
     torch = _torch()
+    for outs in (host_out_flat, host_out_tree):
+        if outs is not None:
+            _one_per_rank(host_ins, outs)
     N = len(host_ins)
     n = host_ins[0].numel()
     dt = host_ins[0].dtype

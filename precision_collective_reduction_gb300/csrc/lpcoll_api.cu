@@ -65,10 +65,16 @@ int full_wave(const void *kernel, int cap)
         if (it != g_wave.end()) {
             sms = it->second.first;
             per_sm = it->second.second;
-        } else {
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+        } else if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ==
+                       cudaSuccess &&
+                   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads,
+                                                                 0) == cudaSuccess) {
             g_wave.emplace(OccKey{kernel, dev}, std::make_pair(sms, per_sm));
+        } else {
+            // not cached: a failed query leaves no error behind and launches
+            // one CTA (the kernels stride over any grid size)
+            cudaGetLastError();
+            return 1;
         }
     }
     if (per_sm > cap)
@@ -174,21 +180,25 @@ int collective_args(const void *const *in, void *const *out, int nranks, int dty
                     int block, uint8_t *const *wire_codes, float *const *wire_scales,
                     Empty out_empty, DdaParams &p)
 {
+    int out_st = LPCOLL_OK;
+    if (out == nullptr) {
+        out_st = LPCOLL_ERR_ARG;
+    } else {
+        for (int r = 0; r < nranks && out_st != LPCOLL_ERR_RANK; ++r) {
+            if (out[r] == nullptr && !out_empty(r))
+                out_st = LPCOLL_ERR_RANK;
+            else if (out[r] != nullptr && misaligned(out[r]))
+                out_st = LPCOLL_ERR_ALIGN;
+        }
+    }
     int st = first_error({
         check_rank_array(in, nranks),
+        out_st,
         block ? check_rank_array(wire_codes, nranks) : LPCOLL_OK,
         block ? check_rank_array(wire_scales, nranks) : LPCOLL_OK,
     });
     if (st != LPCOLL_OK)
         return st;
-    if (out == nullptr)
-        return LPCOLL_ERR_ARG;
-    for (int r = 0; r < nranks; ++r)
-        if (out[r] == nullptr && !out_empty(r))
-            return LPCOLL_ERR_RANK;
-    for (int r = 0; r < nranks; ++r)
-        if (out[r] != nullptr && misaligned(out[r]))
-            return LPCOLL_ERR_ALIGN;
     for (int r = 0; r < nranks; ++r) {
         p.in[r] = in[r];
         p.out[r] = out[r];

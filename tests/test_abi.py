@@ -143,6 +143,10 @@ def test_collective_validation(L, fn):
     assert f(two, two, 2, 10, 1, 128, two, arr(None, A), None) == RANK
     assert f(two, arr(A, A + 4), 2, 10, 0, 0, None, None, None) == ALIGN
     assert f(two, two, 2, 10, 0, 128, arr(A + 2, A), two, None) == ALIGN
+    # a NULL anywhere outranks a misaligned pointer anywhere
+    assert f(arr(A + 4, A), None, 2, 10, 0, 0, None, None, None) == ARG
+    assert f(arr(A + 4, A), arr(A, None), 2, 10, 0, 0, None, None, None) == RANK
+    assert f(two, arr(A + 4, A), 2, 10, 0, 128, arr(A, None), two, None) == RANK
     if fn == "reduce_scatter_sim":
         # n = 10 over 8 ranks: shards of 2 elements, ranks 5..7 empty. Their
         # outputs may be NULL: the call gets past the NULL checks and stops at

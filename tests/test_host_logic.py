@@ -76,3 +76,35 @@ def test_staged_bytes():
     assert bench.staged_bytes("lp_quantize", N, n, 4) == 4 * n + q
     assert bench.staged_bytes("lp_dequantize", N, n, 2) == q + 2 * n
     assert bench.staged_bytes("lp_reduce", N, n, 4) == N * q + 4 * n
+
+
+def test_binding_refuses_short_rank_lists():
+    # the C calls read N entries of every per-rank pointer array: the binding
+    # must refuse a shorter list before it calls the library
+    import torch
+    from precision_collective_reduction_gb300 import _binding as B
+    with pytest.raises(ValueError):
+        B.raw_dda_flat_sim([16, 32], [16], 2, 10, B.F32, 0, [], [], 0)
+    with pytest.raises(ValueError):
+        B.raw_dda_tree_sim([16, 32], [16, 32], 2, 10, B.F32, 128, [16], [16, 32], 16, 16, 0)
+    with pytest.raises(ValueError):
+        B.raw_collective("all_gather_sim", [16], [16, 32], 2, 10, B.F32, 0, [], [], 0)
+    with pytest.raises(ValueError):
+        B.raw_lp_reduce([16, 32, 48], [16, 32], 3, 10, 128, 16, B.F32, 0)
+    with pytest.raises(ValueError):
+        B.raw_dda_flat_sim_noalloc([16], [16], 2, 10, B.F32, 0)
+    with pytest.raises(ValueError):
+        B.raw_host_allreduce([16, 32], [16], None, 2, 10, B.F32, 128, 128, 1, 16, 1 << 20,
+                             0, 0, 0)
+    # tensor-level calls check the list lengths before anything else
+    t = [torch.zeros(4) for _ in range(3)]
+    for fn in (B.dda_flat_sim, B.dda_tree_sim, B.reduce_scatter_sim, B.all_gather_sim,
+               B.all_to_all_sim):
+        with pytest.raises(ValueError):
+            fn(t, t[:2], block=0)
+    with pytest.raises(ValueError):
+        B.dda_flat_sim_noalloc(t, t[:1])
+    with pytest.raises(ValueError):
+        B.lpcoll_host_allreduce(t, host_out_flat=t[:2])
+    with pytest.raises(ValueError):
+        B.dda_flat_sim([], [], block=0)
