@@ -358,6 +358,18 @@ def measure_small(torch, w, stream, iters, graph_replays=0):
         nbytes = bytes_alg(w.nranks, w.n, w.elem_bytes, w.block, algo)
         res = {"us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
                "bytes_alg": nbytes, "l2": "flushed"}
+        # warm L2: back-to-back calls, no flush (what a chain of calls costs)
+        warm_calls = 200
+        with torch.cuda.stream(stream):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(warm_calls):
+                bufs.run(algo, s)
+            b.record(stream)
+        torch.cuda.synchronize()
+        res["warm_us_per_call"] = round(a.elapsed_time(b) * 1e3 / warm_calls, 3)
+        res["warm_calls"] = warm_calls
         if graph_replays:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
