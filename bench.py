@@ -27,6 +27,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -222,14 +223,31 @@ def oracle_pass(w, n):
     return time.perf_counter() - t0
 
 
+def host_cpu():
+    """The host's CPU model (or architecture) and core count."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"host_cpu": model or platform.machine(), "host_cores": os.cpu_count()}
+
+
 def cpu_baseline(w):
     secs = oracle_pass(w, CPU_SAMPLE_ELEMS)
-    return {"value": round(step_bytes(w, CPU_SAMPLE_ELEMS) / secs / 1e9, 4),
-            "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d of the workload's %d elements per rank (same recipe and "
-                      "seed), %d ranks, one flat + one tree pass, single-threaded C "
-                      "oracle (%.1f s)"
-                      % (CPU_SAMPLE_ELEMS, w.n, w.nranks, secs)}
+    res = {"value": round(step_bytes(w, CPU_SAMPLE_ELEMS) / secs / 1e9, 4),
+           "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": "%d of the workload's %d elements per rank (same recipe and "
+                     "seed), %d ranks, one flat + one tree pass, single-threaded C "
+                     "oracle (%.1f s)"
+                     % (CPU_SAMPLE_ELEMS, w.n, w.nranks, secs)}
+    res.update(host_cpu())
+    return res
 
 
 def run_reference(args):
@@ -254,7 +272,7 @@ def run_reference(args):
                          "kind": "oracle",
                          "sample": "%d of the workload's %d elements per rank (same "
                                    "recipe and seed), %d ranks, flat + tree per step"
-                                   % (n, w.n, w.nranks)},
+                                   % (n, w.n, w.nranks), **host_cpu()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
