@@ -40,12 +40,17 @@ thread_local int g_last_cuda_error = 0;
 struct OccKey {
     const void *fn;
     int dev;
-    bool operator==(const OccKey &o) const { return fn == o.fn && dev == o.dev; }
+    size_t smem;
+    bool operator==(const OccKey &o) const
+    {
+        return fn == o.fn && dev == o.dev && smem == o.smem;
+    }
 };
 struct OccHash {
     size_t operator()(const OccKey &k) const
     {
-        return std::hash<const void *>()(k.fn) ^ (static_cast<size_t>(k.dev) << 1);
+        return std::hash<const void *>()(k.fn) ^ (static_cast<size_t>(k.dev) << 1) ^
+               (k.smem << 7);
     }
 };
 
@@ -53,30 +58,35 @@ std::mutex g_occ_mutex;
 // SM count and resident CTAs per SM of each kernel on each device
 std::unordered_map<OccKey, std::pair<int, int>, OccHash> g_wave;
 
-int full_wave(const void *kernel, int cap)
+// SM count and resident CTAs per SM of kernel (0, 0 if the queries fail).
+std::pair<int, int> occupancy(const void *kernel, size_t smem)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return 1;
-    int sms = 0, per_sm = 0;
-    {
-        std::lock_guard<std::mutex> lock(g_occ_mutex);
-        auto it = g_wave.find(OccKey{kernel, dev});
-        if (it != g_wave.end()) {
-            sms = it->second.first;
-            per_sm = it->second.second;
-        } else if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ==
-                       cudaSuccess &&
-                   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads,
-                                                                 0) == cudaSuccess) {
-            g_wave.emplace(OccKey{kernel, dev}, std::make_pair(sms, per_sm));
-        } else {
-            // not cached: a failed query leaves no error behind and launches
-            // one CTA (the kernels stride over any grid size)
-            cudaGetLastError();
-            return 1;
-        }
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return {0, 0};
     }
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    auto it = g_wave.find(OccKey{kernel, dev, smem});
+    if (it != g_wave.end())
+        return it->second;
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) !=
+            cudaSuccess) {
+        // not cached, and no error left behind
+        cudaGetLastError();
+        return {0, 0};
+    }
+    g_wave.emplace(OccKey{kernel, dev, smem}, std::make_pair(sms, per_sm));
+    return {sms, per_sm};
+}
+
+int full_wave(const void *kernel, int cap, size_t smem)
+{
+    const std::pair<int, int> occ = occupancy(kernel, smem);
+    const int sms = occ.first;
+    int per_sm = occ.second;
     if (per_sm > cap)
         per_sm = cap;
     const int wave = sms * per_sm;
@@ -233,10 +243,12 @@ int check_common(int dtype, int nranks, int block)
 
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
 
-int wave_ctas(const void *kernel, size_t units, int cap)
+int resident_ctas(const void *kernel, size_t smem) { return occupancy(kernel, smem).second; }
+
+int wave_ctas(const void *kernel, size_t units, int cap, size_t smem)
 {
     const size_t need = (units + kWarpsPerCta - 1) / kWarpsPerCta;
-    const size_t wave = static_cast<size_t>(full_wave(kernel, cap));
+    const size_t wave = static_cast<size_t>(full_wave(kernel, cap, smem));
     const size_t g = need < wave ? need : wave;
     return static_cast<int>(g < 1 ? 1 : g);
 }

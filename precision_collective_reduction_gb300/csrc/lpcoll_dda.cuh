@@ -21,6 +21,14 @@
 // per SM for large allreduces and 4 otherwise (kCtasPerSm / kCtasPerSmBusy),
 // all resident at once, so the units of every rank stream through HBM in
 // order.
+//
+// Tile path (TILES; see tile_path_built for where it is used): a CTA
+// instead takes a tile of kTileUnits consecutive units per iteration (one
+// per warp), builds the tile's outputs, codes and scales in a double-buffered
+// shared-memory area, and one thread writes each of them with a single bulk
+// copy (cp.async.bulk.global.shared::cta). The loads and the arithmetic are
+// the same as on the direct path; only where the results go differs (the
+// sink), so both paths give bit-identical results.
 #pragma once
 
 #include "lpcoll_device.cuh"
@@ -76,16 +84,100 @@ __device__ __forceinline__ void load_unit(const DdaParams &p, size_t e0, int cnt
                                    : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Everything after the loads: quantize / dequantize / reduce / requantize,
-// then the output stores.
+// Where a unit's results go. GlobalSink stores them straight to the
+// caller's buffers (cnt valid elements at e0; FULL: cnt == kVec). TileSink
+// writes them into the CTA's shared-memory tile, at the lane's element
+// offset `off` within the tile, for the bulk copies that follow.
 template <int N, int DT, int MODE, bool FULL>
-__device__ __forceinline__ void process_unit(const DdaParams &p, size_t e0, int cnt,
-                                             int lane, const uint4 (&raw)[N])
+struct GlobalSink {
+    const DdaParams &p;
+    size_t e0;
+    int cnt;
+    __device__ __forceinline__ bool live() const { return FULL || cnt > 0; }
+    __device__ __forceinline__ void codes(int r, Codes<DT> c) const
+    {
+        store_codes(p.codes[r], e0, cnt, c);
+    }
+    __device__ __forceinline__ void scale(int r, float s) const
+    {
+        __stcs(p.scales[r] + e0 / kBlock, s);
+    }
+    __device__ __forceinline__ void shard_codes(Codes<DT> c) const
+    {
+        store_codes(p.shard_codes, e0, cnt, c);
+    }
+    __device__ __forceinline__ void shard_scale(float s) const
+    {
+        __stcs(p.shard_scales + e0 / kBlock, s);
+    }
+    __device__ __forceinline__ void out(uint4 o) const
+    {
+        if constexpr (MODE == kScatterExact || MODE == kScatterLp) {
+            scatter_store<DT>(p, e0, cnt, o);
+        } else {
+#pragma unroll
+            for (int r = 0; r < N; ++r)
+                store_vec<DT>(p.out[r], e0, cnt, o);
+        }
+    }
+};
+
+// Byte layout of one shared-memory tile buffer (kTileUnits units of every
+// rank): the result, then per rank the codes and the scales, then the tree's
+// shard codes and scales. Every part starts 16-byte aligned, as the bulk
+// copies need.
+constexpr int kTileUnits = kWarpsPerCta;
+template <int N, int DT>
+struct TileLayout {
+    static constexpr int kElems = kTileUnits * 32 * Fmt<DT>::kVec;  // 1024 / 2048
+    static constexpr int kBlocks = kElems / kBlock;
+    static constexpr int kRes = 0;
+    static constexpr int kCodes = kRes + kElems * (16 / Fmt<DT>::kVec);
+    static constexpr int kScales = kCodes + N * kElems;
+    static constexpr int kShardCodes = kScales + N * kBlocks * 4;
+    static constexpr int kShardScales = kShardCodes + kElems;
+    static constexpr int kBytes = kShardScales + kBlocks * 4;
+    static_assert(kCodes % 16 == 0 && kScales % 16 == 0 && kShardCodes % 16 == 0 &&
+                      kShardScales % 16 == 0 && kBytes % 16 == 0 && (kBlocks * 4) % 16 == 0,
+                  "tile parts must be 16-byte aligned for bulk copies");
+};
+
+template <int N, int DT>
+struct TileSink {
+    using L = TileLayout<N, DT>;
+    unsigned char *tile;
+    int off;  // element offset of this lane's first element in the tile
+    __device__ __forceinline__ bool live() const { return true; }
+    __device__ __forceinline__ void codes(int r, Codes<DT> c) const
+    {
+        *reinterpret_cast<Codes<DT> *>(tile + L::kCodes + r * L::kElems + off) = c;
+    }
+    __device__ __forceinline__ void scale(int r, float s) const
+    {
+        reinterpret_cast<float *>(tile + L::kScales)[r * L::kBlocks + off / kBlock] = s;
+    }
+    __device__ __forceinline__ void shard_codes(Codes<DT> c) const
+    {
+        *reinterpret_cast<Codes<DT> *>(tile + L::kShardCodes + off) = c;
+    }
+    __device__ __forceinline__ void shard_scale(float s) const
+    {
+        reinterpret_cast<float *>(tile + L::kShardScales)[off / kBlock] = s;
+    }
+    __device__ __forceinline__ void out(uint4 o) const
+    {
+        *reinterpret_cast<uint4 *>(tile + L::kRes + off * (16 / Fmt<DT>::kVec)) = o;
+    }
+};
+
+// Everything after the loads: quantize / dequantize / reduce / requantize,
+// then the results to the sink.
+template <int N, int DT, int MODE, class Sink>
+__device__ __forceinline__ void process_unit(const Sink &sink, int lane, const uint4 (&raw)[N])
 {
     using F = Fmt<DT>;
     constexpr int V = F::kVec;
     constexpr bool kExactSum = (MODE == kExact || MODE == kScatterExact);
-    constexpr bool kScatter = (MODE == kScatterExact || MODE == kScatterLp);
     const bool leader = (lane % F::kGroup) == 0;
 
     float acc[V];
@@ -100,10 +192,10 @@ __device__ __forceinline__ void process_unit(const DdaParams &p, size_t e0, int 
         } else {
             float s;
             Codes<DT> c = quantize_lane<DT>(x, s);
-            if (FULL || cnt > 0) {
-                store_codes(p.codes[r], e0, cnt, c);
+            if (sink.live()) {
+                sink.codes(r, c);
                 if (leader)
-                    __stcs(p.scales[r] + e0 / kBlock, s);
+                    sink.scale(r, s);
             }
             float v[V];
             dequantize_lane<DT>(c, s, v);
@@ -116,24 +208,16 @@ __device__ __forceinline__ void process_unit(const DdaParams &p, size_t e0, int 
     if constexpr (MODE == kTree) {
         float s;
         Codes<DT> c = quantize_lane<DT>(acc, s);
-        if (FULL || cnt > 0) {
-            store_codes(p.shard_codes, e0, cnt, c);
+        if (sink.live()) {
+            sink.shard_codes(c);
             if (leader)
-                __stcs(p.shard_scales + e0 / kBlock, s);
+                sink.shard_scale(s);
         }
         dequantize_lane<DT>(c, s, acc);
     }
 
-    if (FULL || cnt > 0) {
-        const uint4 o = narrow<DT>(acc);
-        if constexpr (kScatter) {
-            scatter_store<DT>(p, e0, cnt, o);
-        } else {
-#pragma unroll
-            for (int r = 0; r < N; ++r)
-                store_vec<DT>(p.out[r], e0, cnt, o);
-        }
-    }
+    if (sink.live())
+        sink.out(narrow<DT>(acc));
 }
 
 template <int N, int DT, int MODE, bool FULL>
@@ -145,7 +229,7 @@ __device__ __forceinline__ void dda_unit(const DdaParams &p, size_t n, size_t un
     const int cnt = FULL ? V : lane_count<DT>(n, e0);
     uint4 raw[N];
     load_unit<N, DT, FULL>(p, e0, cnt, raw);
-    process_unit<N, DT, MODE, FULL>(p, e0, cnt, lane, raw);
+    process_unit<N, DT, MODE>(GlobalSink<N, DT, MODE, FULL>{p, e0, cnt}, lane, raw);
 }
 
 // K consecutive full units, all K x N loads issued before any processing.
@@ -159,15 +243,89 @@ __device__ __forceinline__ void dda_units(const DdaParams &p, size_t unit0, int 
         load_unit<N, DT, true>(p, ((unit0 + k) * 32 + lane) * V, V, raw[k]);
 #pragma unroll
     for (int k = 0; k < K; ++k)
-        process_unit<N, DT, MODE, true>(p, ((unit0 + k) * 32 + lane) * V, V, lane, raw[k]);
+        process_unit<N, DT, MODE>(
+            GlobalSink<N, DT, MODE, true>{p, ((unit0 + k) * 32 + lane) * V, V}, lane, raw[k]);
 }
 
+// One thread's bulk copy of `bytes` from shared to global memory; its
+// completion is tracked with commit / wait groups.
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(static_cast<uint32_t>(__cvta_generic_to_shared(ssrc))), "r"(bytes)
+                 : "memory");
+}
+
+// Tile path. Full tiles (kTileUnits consecutive full units) go through the
+// CTA's shared-memory tile and bulk copies, two tile buffers alternating;
+// the units after the last full tile (fewer than kTileUnits full ones and
+// the ragged one) take the direct path.
 template <int N, int DT, int MODE>
+__device__ __forceinline__ void dda_tiles(const DdaParams &p, size_t n, size_t full_units,
+                                          size_t total_units)
+{
+    using L = TileLayout<N, DT>;
+    constexpr int V = Fmt<DT>::kVec;
+    constexpr int ES = 16 / V;
+    extern __shared__ __align__(128) unsigned char tile_smem[];
+    const int lane = threadIdx.x & 31;
+    const int w = threadIdx.x >> 5;
+    const size_t tiles = full_units / kTileUnits;
+    size_t i = 0;
+    for (size_t t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+        unsigned char *tile = tile_smem + (i & 1) * L::kBytes;
+        if (threadIdx.x == 0)  // the copies of two tiles ago have read this buffer
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncthreads();
+        const size_t e0 = ((t * kTileUnits + w) * 32 + lane) * V;
+        uint4 raw[N];
+        load_unit<N, DT, true>(p, e0, V, raw);
+        process_unit<N, DT, MODE>(TileSink<N, DT>{tile, (w * 32 + lane) * V}, lane, raw);
+        // the tile's generic-proxy writes must be visible to the bulk copies
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const size_t eb = t * L::kElems;  // first element of the tile
+            for (int r = 0; r < N; ++r)
+                bulk_store(static_cast<char *>(p.out[r]) + eb * ES, tile + L::kRes,
+                           L::kElems * ES);
+            if constexpr (MODE != kExact) {
+                for (int r = 0; r < N; ++r) {
+                    bulk_store(p.codes[r] + eb, tile + L::kCodes + r * L::kElems, L::kElems);
+                    bulk_store(p.scales[r] + eb / kBlock, tile + L::kScales + r * L::kBlocks * 4,
+                               L::kBlocks * 4);
+                }
+            }
+            if constexpr (MODE == kTree) {
+                bulk_store(p.shard_codes + eb, tile + L::kShardCodes, L::kElems);
+                bulk_store(p.shard_scales + eb / kBlock, tile + L::kShardScales,
+                           L::kBlocks * 4);
+            }
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+    }
+    const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
+    const size_t u0 = tiles * kTileUnits;
+    for (size_t u = u0 + warp; u < full_units; u += nwarps)
+        dda_unit<N, DT, MODE, true>(p, n, u, lane);
+    if (total_units > full_units && warp == (full_units - u0) % nwarps)
+        dda_unit<N, DT, MODE, false>(p, n, full_units, lane);
+    // the copies must have read the tiles (and landed) before the CTA exits
+    if (threadIdx.x == 0)
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+template <int N, int DT, int MODE, bool TILES>
 __global__ void __launch_bounds__(kThreads)
 dda_kernel(const __grid_constant__ DdaParams p, size_t n, size_t full_units,
            size_t total_units)
 {
     wait_prior_grid();
+    if constexpr (TILES) {
+        dda_tiles<N, DT, MODE>(p, n, full_units, total_units);
+        return;
+    }
     constexpr int K = units_per_iter<N>();
     const int lane = threadIdx.x & 31;
     const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
@@ -197,21 +355,57 @@ inline void unit_counts(size_t n, size_t &full, size_t &total)
 }
 
 // CTAs for a launch covering `units` warp-units: enough for every unit, at
-// most min(resident CTAs per SM, cap) x SMs.
-int wave_ctas(const void *kernel, size_t units, int cap = kCtasPerSmBusy);
+// most min(resident CTAs per SM, cap) x SMs (occupancy with `smem` bytes of
+// dynamic shared memory per CTA).
+int wave_ctas(const void *kernel, size_t units, int cap = kCtasPerSmBusy, size_t smem = 0);
+
+// Resident CTAs per SM of a kernel with `smem` bytes of dynamic shared
+// memory (cached per kernel, device and size).
+int resident_ctas(const void *kernel, size_t smem);
+
+// Tile path policy, from measurements on GB300 (CUDA events, L2 flushed,
+// LP, tile path against the direct path):
+//   FP32, 8 ranks: 256 MiB of input 97.8 -> 100.4 us (flat), 512 MiB equal,
+//     1 GiB 381.5 -> 372.8 us, 2 GiB 761.6 -> 733.4 us (flat) and
+//     783.9 -> 760.9 us (tree), 4 GiB 1513 -> 1460 us;
+//   FP32, 12 ranks: 3-7% slower at every size from 256 MiB to 4 GiB;
+//   FP32, 16 ranks: 7-11% slower (98 registers leave 2 CTAs per SM);
+//   FP32, 4 ranks (4 loads per lane instead of the direct path's 8): 7% slower;
+//   BF16, 8 ranks, 128 and 512 MiB: equal; the exact allreduce: equal.
+// So it is taken for FP32 LP allreduces of 8 ranks and 1 GiB of input or
+// more, when kTileCtasPerSm CTAs fit on an SM; everything else stays direct.
+constexpr int kTileCtasPerSm = 3;
+constexpr size_t kTileMinBytes = size_t(1) << 30;
+template <int N, int DT, int MODE>
+constexpr bool tile_path_built()
+{
+    return (MODE == kFlat || MODE == kTree) && DT == LPCOLL_F32 && N == 8;
+}
 
 template <int N, int DT, int MODE>
 cudaError_t launch_dda_n(const DdaParams &p, size_t n, cudaStream_t stream)
 {
     size_t full, total;
     unit_counts<DT>(n, full, total);
-    const void *k = reinterpret_cast<const void *>(&dda_kernel<N, DT, MODE>);
+    if constexpr (tile_path_built<N, DT, MODE>()) {
+        const size_t bytes = n * static_cast<size_t>(N) * (16 / Fmt<DT>::kVec);
+        const size_t tiles = full / kTileUnits;
+        constexpr size_t smem = 2 * static_cast<size_t>(TileLayout<N, DT>::kBytes);
+        static_assert(smem <= 48 * 1024, "tile buffers must fit the default dynamic smem");
+        auto *kt = &dda_kernel<N, DT, MODE, true>;
+        const void *ktv = reinterpret_cast<const void *>(kt);
+        if (bytes >= kTileMinBytes && tiles > 0 && resident_ctas(ktv, smem) >= kTileCtasPerSm) {
+            const int grid = wave_ctas(ktv, tiles * kWarpsPerCta, kTileCtasPerSm, smem);
+            return launch_kernel_smem(kt, grid, smem, stream, p, n, full, total);
+        }
+    }
+    const void *k = reinterpret_cast<const void *>(&dda_kernel<N, DT, MODE, false>);
     const size_t K = units_per_iter<N>();
     const bool scatter = (MODE == kScatterExact || MODE == kScatterLp);
     const size_t in_bytes = n * static_cast<size_t>(N) * (16 / Fmt<DT>::kVec);
     const int cap = (scatter || in_bytes < kSmallLaunchBytes) ? kCtasPerSmBusy : kCtasPerSm;
     const int grid = wave_ctas(k, (total + K - 1) / K, cap);
-    return launch_kernel(dda_kernel<N, DT, MODE>, grid, stream, p, n, full, total);
+    return launch_kernel(dda_kernel<N, DT, MODE, false>, grid, stream, p, n, full, total);
 }
 
 template <int DT, int MODE>

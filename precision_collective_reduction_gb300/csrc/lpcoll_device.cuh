@@ -55,8 +55,8 @@ __device__ __forceinline__ void wait_prior_grid()
 }
 
 template <typename... Params, typename... Args>
-cudaError_t launch_kernel(void (*kernel)(Params...), int grid, cudaStream_t stream,
-                          Args... args)
+cudaError_t launch_kernel_smem(void (*kernel)(Params...), int grid, size_t smem,
+                               cudaStream_t stream, Args... args)
 {
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -64,11 +64,18 @@ cudaError_t launch_kernel(void (*kernel)(Params...), int grid, cudaStream_t stre
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(Params...), int grid, cudaStream_t stream,
+                          Args... args)
+{
+    return launch_kernel_smem(kernel, grid, 0, stream, args...);
 }
 
 // What a fused launch computes: the allreduce (exact, LP flat, LP tree) or a

@@ -154,6 +154,20 @@ def test_staged_many_grid_passes(oracle, dt):
 
 # -- fused allreduce ------------------------------------------------------------
 
+@pytest.mark.parametrize("algo,in_place", [("flat", False), ("tree", False), ("tree", True)])
+def test_tile_path_full_oracle(oracle, algo, in_place):
+    """FP32 low-precision allreduces of 8 ranks and 1 GiB of input or more
+    take the tile path (results staged in shared memory, written by bulk
+    copies): every element, code and scale against the oracle, with full
+    tiles, a few full units after them and a ragged last unit."""
+    N, n = 8, (1 << 25) + 3 * 1024 + 77
+    assert N * n * 4 >= 1 << 30
+    ins = W.random_inputs(N, n, F32, 9100 + in_place, scale_spread=3.0)
+    res = gpu_allreduce(ins, algo, block=128, in_place=in_place)
+    check_against_oracle(oracle, ins, algo, 128, res)
+
+
+
 @pytest.mark.parametrize("algo", ["flat", "tree"])
 @pytest.mark.parametrize("block", [128, 0])
 @pytest.mark.parametrize("dt", [F32, BF16])
