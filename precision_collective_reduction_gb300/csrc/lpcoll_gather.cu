@@ -1,7 +1,10 @@
 // lpcoll_gather.cu -- the collectives without a reduction: AllGather and
 // AlltoAll over N emulated ranks, exact or low precision.
 //
-// AllGather and the exact AlltoAll: each warp takes an item of kItemUnits
+// The low-precision AllGather of 16-byte-aligned contributions runs on
+// tiles staged in shared memory and written with bulk copies
+// (gather_tile_kernel). The exact AllGather (and the LP one at unaligned
+// lengths) and the exact AlltoAll: each warp takes an item of kItemUnits
 // consecutive units (32 x kVec elements each) of one sender's data: it loads
 // them all, and in low precision quantizes them on the sender's blocks (one
 // absmax scale per 128 elements counted from the start of what the sender
@@ -19,6 +22,8 @@
 // Offsets that are not 16-byte aligned (a contribution or chunk length that
 // is not a multiple of 16 bytes) take the element-by-element path for the
 // accesses that need it; the choice is made once per launch (ALIGNED).
+#include <algorithm>
+
 #include "lpcoll_dda.cuh"
 #include "lpcoll_device.cuh"
 #include "lpcoll_wide.cuh"
@@ -107,6 +112,106 @@ gather_kernel(const __grid_constant__ DdaParams p, int nranks, size_t m, size_t 
         gather_item<DT, LP, ALIGNED>(p, nranks, m, r, it - static_cast<size_t>(r) * groups,
                                      lane);
     }
+}
+
+// Low-precision AllGather of contributions whose byte length is a multiple
+// of 16 (every output offset then 16-byte aligned): a CTA takes a tile of
+// kWarpsPerCta consecutive units of one sender (one per warp), quantizes and
+// dequantizes it into one of two shared-memory tile buffers, and one thread
+// writes the tile to all N receivers, and its codes and scales to the
+// sender's wire, with bulk copies (cp.async.bulk.global.shared::cta); the
+// units after a sender's last full tile are stored directly. Measured on
+// GB300 against the item kernel above (8 ranks, CUDA events, L2 flushed):
+// 1 Mi BF16 contributions 28.7 -> 28.7 us, 4 Mi BF16 108.5 -> 102.4 us,
+// 8 Mi FP32 420.1 -> 386.7 us (6427 GB/s); 3 CTAs per SM (2 or 4: 3-6%
+// slower), one unit per warp (2 or 4 units: slower above 1 Mi).
+constexpr int kAgTileCtasPerSm = 3;
+template <int DT>
+struct AgTile {
+    static constexpr int kUnits = kWarpsPerCta;
+    static constexpr int kElems = kUnits * 32 * Fmt<DT>::kVec;
+    static constexpr int kBlocks = kElems / kBlock;
+    static constexpr int kRes = 0;
+    static constexpr int kCodes = kElems * (16 / Fmt<DT>::kVec);
+    static constexpr int kScales = kCodes + kElems;
+    static constexpr int kBytes = kScales + kBlocks * 4;
+    static_assert(kCodes % 16 == 0 && kScales % 16 == 0 && kBytes % 16 == 0 &&
+                      (kBlocks * 4) % 16 == 0,
+                  "tile parts must be 16-byte aligned for bulk copies");
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads)
+gather_tile_kernel(const __grid_constant__ DdaParams p, int nranks, size_t m,
+                   size_t tiles_per_sender, size_t units_per_sender)
+{
+    wait_prior_grid();
+    using L = AgTile<DT>;
+    constexpr int V = Fmt<DT>::kVec;
+    constexpr int ES = 16 / V;
+    extern __shared__ __align__(128) unsigned char ag_smem[];
+    const int lane = threadIdx.x & 31;
+    const int w = threadIdx.x >> 5;
+    const size_t tiles = static_cast<size_t>(nranks) * tiles_per_sender;
+    size_t i = 0;
+    for (size_t t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+        const int r = static_cast<int>(t / tiles_per_sender);
+        const size_t tt = t - static_cast<size_t>(r) * tiles_per_sender;
+        unsigned char *tile = ag_smem + (i & 1) * L::kBytes;
+        if (threadIdx.x == 0)  // the copies of two tiles ago have read this buffer
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncthreads();
+        const size_t e0 = ((tt * L::kUnits + w) * 32 + lane) * V;
+        const int off = (w * 32 + lane) * V;
+        float x[V];
+        widen<DT>(load_vec<DT>(p.in[r], e0, V), x);
+        float s;
+        const Codes<DT> c = quantize_lane<DT>(x, s);
+        *reinterpret_cast<Codes<DT> *>(tile + L::kCodes + off) = c;
+        if ((lane % Fmt<DT>::kGroup) == 0)
+            reinterpret_cast<float *>(tile + L::kScales)[off / kBlock] = s;
+        dequantize_lane<DT>(c, s, x);
+        *reinterpret_cast<uint4 *>(tile + L::kRes + off * ES) = narrow<DT>(x);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const size_t eb = tt * L::kElems;
+            const size_t at = static_cast<size_t>(r) * m + eb;
+            for (int d = 0; d < nranks; ++d)
+                bulk_store(static_cast<char *>(p.out[d]) + at * ES, tile + L::kRes,
+                           L::kElems * ES);
+            bulk_store(p.codes[r] + eb, tile + L::kCodes, L::kElems);
+            bulk_store(p.scales[r] + eb / kBlock, tile + L::kScales, L::kBlocks * 4);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+    }
+    // the units after each sender's full tiles (the ragged one included),
+    // one per warp, stored directly
+    const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
+    const size_t u0 = tiles_per_sender * L::kUnits;
+    const size_t tail = units_per_sender - u0;
+    for (size_t it = warp; it < static_cast<size_t>(nranks) * tail; it += nwarps) {
+        const int r = static_cast<int>(it / tail);
+        const size_t u = u0 + (it - static_cast<size_t>(r) * tail);
+        const size_t e0 = (u * 32 + lane) * V;
+        const int cnt = lane_count<DT>(m, e0);
+        float x[V];
+        widen<DT>(cnt > 0 ? load_vec<DT>(p.in[r], e0, cnt) : make_uint4(0u, 0u, 0u, 0u), x);
+        float s;
+        const Codes<DT> c = quantize_lane<DT>(x, s);
+        dequantize_lane<DT>(c, s, x);
+        if (cnt > 0) {
+            store_codes(p.codes[r], e0, cnt, c);
+            if ((lane % Fmt<DT>::kGroup) == 0)
+                __stcs(p.scales[r] + e0 / kBlock, s);
+            const uint4 o = narrow<DT>(x);
+            for (int d = 0; d < nranks; ++d)
+                store_vec<DT>(p.out[d], static_cast<size_t>(r) * m + e0, cnt, o);
+        }
+    }
+    if (threadIdx.x == 0)  // the copies must have completed before the CTA exits
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // One item of chunk j (c elements) of sender r in the exact AlltoAll.
@@ -244,6 +349,22 @@ inline size_t item_groups(size_t len)
 template <int DT, bool LP, bool ALIGNED>
 cudaError_t launch_gather_t(const DdaParams &p, int nranks, size_t m, cudaStream_t st)
 {
+    if constexpr (LP && ALIGNED) {
+        using L = AgTile<DT>;
+        size_t full, units;
+        unit_counts<DT>(m, full, units);
+        const size_t tps = full / L::kUnits;
+        constexpr size_t smem = 2 * static_cast<size_t>(L::kBytes);
+        static_assert(smem <= 48 * 1024, "tile buffers must fit the default dynamic smem");
+        // one CTA per tile, or enough warps for the units after the tiles
+        const size_t tail_units = static_cast<size_t>(nranks) * (units - tps * L::kUnits);
+        const size_t need = std::max(static_cast<size_t>(nranks) * tps,
+                                     (tail_units + kWarpsPerCta - 1) / kWarpsPerCta);
+        auto *k = &gather_tile_kernel<DT>;
+        const int grid = wave_ctas(reinterpret_cast<const void *>(k), need * kWarpsPerCta,
+                                   kAgTileCtasPerSm, smem);
+        return launch_kernel_smem(k, grid, smem, st, p, nranks, m, tps, units);
+    }
     const size_t groups = item_groups<DT>(m);
     const void *k = reinterpret_cast<const void *>(&gather_kernel<DT, LP, ALIGNED>);
     const int grid = wave_ctas(k, groups * static_cast<size_t>(nranks));

@@ -61,7 +61,7 @@ def test_reduce_scatter(oracle, dt, block, N, n):
 @pytest.mark.parametrize("dt", [W.F32, W.BF16])
 @pytest.mark.parametrize("block", [128, 0])
 @pytest.mark.parametrize("N", [1, 3, 8, 16])
-@pytest.mark.parametrize("m", [1, 3, 77, 128, 200, 1000, 4096 + 77, 32 * 8 * 20])
+@pytest.mark.parametrize("m", [1, 3, 77, 128, 200, 1000, 4096 + 77, 32 * 8 * 20, 3 * 1024 + 264])
 def test_all_gather(oracle, dt, block, N, m):
     ins = W.random_inputs(N, m, dt, 9500 + 11 * N + m, scale_spread=3.0)
     outs = [Guarded(N * m, TDT[dt]) for _ in range(N)]
