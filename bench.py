@@ -235,6 +235,16 @@ def host_cpu():
                     break
     except OSError:
         pass
+    if not model:
+        # Arm hosts list no model name in /proc/cpuinfo; lscpu has it
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
     return {"host_cpu": model or platform.machine(), "host_cores": os.cpu_count()}
 
 
