@@ -41,6 +41,12 @@
  *     while the previous kernel of the stream still runs, but it touches no
  *     memory before that kernel has completed, so stream order holds for
  *     every buffer, also inside CUDA graph capture.
+ *   - Resources: kernels of 256 threads, grids of at most 4 CTAs per SM.
+ *     FP32 low-precision allreduces of 8 ranks with 1 GiB of input or more,
+ *     and low-precision all-gathers of 16-byte-aligned contributions, stage
+ *     results in up to 46 KB of dynamic shared memory per CTA and write
+ *     them with bulk (TMA) copies; every copy has completed when the
+ *     kernel does.
  *   - Return value: LPCOLL_OK, or an lpcoll_status error found before any
  *     launch (nothing is enqueued then), or LPCOLL_ERR_CUDA if the launch
  *     itself failed (lpcoll_last_cuda_error() gives the cudaError_t).
