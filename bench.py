@@ -41,6 +41,7 @@ if ROOT not in sys.path:
 from precision_collective_reduction_gb300 import workloads as W  # noqa: E402
 
 HEADLINE = W.LP_GRAD_N8_256MB_F32
+NOMINAL_HBM_GBS = 7900.0
 METRIC = "LP allreduce-emulation GB/s"
 CPU_SAMPLE_ELEMS = 1 << 23      # cpu_baseline: 8 Mi elements per rank, same recipe
 REF_BUDGET_ELEMS = 1 << 25      # reference arm: elements per rank over all steps
@@ -704,6 +705,8 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(w, world),
         "hbm_frac": round(value / world / peak, 4),
+        # the same against GB300's nominal HBM3e bandwidth (7.9 TB/s)
+        "hbm_frac_nominal": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": roofline, "kernels": kernels,
         "e2e": e2e, "gpu_launches": len(w.algos) * args.steps,
         "clocks": clock_info,
