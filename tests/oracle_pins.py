@@ -386,6 +386,23 @@ def pin_fixed_order(oracle):
         ins.append(x)
     outs, _, _ = oracle.flat(ins)
     assert all(o[5] == np.float32(2.0 ** 24) for o in outs), outs[0][5]
+    # the payload-level reductions, codes and scales written by hand: rank 0
+    # decodes to 1.0 (the code of 1.0 with scale 1), ranks 1 and 2 to 2^-24
+    # (the same code with scale 2^-24). Rank order gives 1.0, the reverse
+    # order 1 + 2^-23: for the main reduce and for every format and block
+    # size of the variants.
+    one = {E4M3: 0x38, E5M2: 0x3C}  # sign 0, exponent = bias, mantissa 0
+    for fmt, block in [(f, b) for f in (E4M3, E5M2) for b in (32, 64, 128, 256)] + [(None, 128)]:
+        n = block + 3
+        nb = -(-n // block)
+        code = one[E4M3 if fmt is None else fmt]
+        codes = [np.full(n, code, dtype=np.uint8) for _ in range(3)]
+        scales = [np.full(nb, s, dtype=np.float32) for s in (1.0, e, e)]
+        for order, want in ((slice(None), 1.0), (slice(None, None, -1), 1.0 + 2.0 ** -23)):
+            cs, ss = codes[order], scales[order]
+            out = (oracle.reduce(cs, ss) if fmt is None
+                   else oracle.reduce_fmt(cs, ss, block, fmt))
+            assert np.all(out == np.float32(want)), (fmt, block, want, out[:3])
 
 
 def _bounds(ins, scales, out_dtype, tree_scales=None):

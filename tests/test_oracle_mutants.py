@@ -65,6 +65,12 @@ MUTANTS = [
     ("e5m2_saturates_to_inf", "        return sign | 0x7B;", "        return sign | 0x7C;"),
     ("variant_block_fixed", "        len = (n - lo < (size_t)block) ? n - lo : (size_t)block;\n        for (i = 0; i < len; i++)\n            buf[i] = load_elem(in, dtype, lo + i);\n        scales[b] = quantize_block_fmt(buf, len, codes + lo, fmt);",
      "        len = (n - lo < (size_t)block) ? n - lo : (size_t)block;\n        for (i = 0; i < len; i++)\n            buf[i] = load_elem(in, dtype, lo + i);\n        scales[b] = quantize_block_fmt(buf, len, codes + lo, block == 256 ? 0 : fmt);"),
+    ("fmt_reduce_drop_last_rank",
+     "        for (r = 1; r < nranks; r++)\n            sum = sum + dequant_elem_fmt(codes[r], scales[r], block, i, fmt);",
+     "        for (r = 1; r < nranks - 1; r++)\n            sum = sum + dequant_elem_fmt(codes[r], scales[r], block, i, fmt);"),
+    ("fmt_reduce_reversed",
+     "        float sum = dequant_elem_fmt(codes[0], scales[0], block, i, fmt);\n        for (r = 1; r < nranks; r++)\n            sum = sum + dequant_elem_fmt(codes[r], scales[r], block, i, fmt);",
+     "        float sum = dequant_elem_fmt(codes[nranks - 1], scales[nranks - 1], block, i, fmt);\n        for (r = nranks - 2; r >= 0; r--)\n            sum = sum + dequant_elem_fmt(codes[r], scales[r], block, i, fmt);"),
     ("a2a_global_blocks",
      "                st = orc_quantize(elem_ptr(in[r], dtype, (size_t)j * c), dtype, c, block,\n                                  wire_codes[r] + (size_t)j * c,\n                                  wire_scales[r] + (size_t)j * nbc);",
      "                st = j ? 0 : orc_quantize(in[r], dtype, c * (size_t)nranks, block,\n                                          wire_codes[r], wire_scales[r]);"),
