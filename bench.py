@@ -361,6 +361,26 @@ def flush_l2(torch, scratch):
     scratch.sum()
 
 
+def flushed_median_us(torch, stream, scratch, fn, iters, warmup=3):
+    """Median microseconds of fn() over `iters` calls on `stream`, each after
+    an L2 flush, timed with CUDA events recorded on that stream; `warmup`
+    untimed calls first."""
+    for _ in range(warmup):
+        fn()
+    times = []
+    with torch.cuda.stream(stream):
+        for _ in range(iters):
+            flush_l2(torch, scratch)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b) * 1e3)
+    return statistics.median(times)
+
+
 def measure_small(torch, w, stream, iters, graph_replays=0):
     """us per call of workload w (median of iters, L2 flushed before each)."""
     from precision_collective_reduction_gb300 import runner
@@ -370,20 +390,7 @@ def measure_small(torch, w, stream, iters, graph_replays=0):
     s = stream.cuda_stream
     out = {}
     for algo in w.algos:
-        for _ in range(3):
-            bufs.run(algo, s)
-        times = []
-        with torch.cuda.stream(stream):
-            for _ in range(iters):
-                flush_l2(torch, scratch)
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                bufs.run(algo, s)
-                b.record(stream)
-                b.synchronize()
-                times.append(a.elapsed_time(b) * 1e3)
-        us = statistics.median(times)
+        us = flushed_median_us(torch, stream, scratch, lambda: bufs.run(algo, s), iters)
         nbytes = bytes_alg(w.nranks, w.n, w.elem_bytes, w.block, algo)
         res = {"us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
                "bytes_alg": nbytes, "l2": "flushed"}
@@ -466,20 +473,7 @@ def measure_collectives(torch, stream, iters=20):
     }
     out = {}
     for kind, (fn, count) in calls.items():
-        for _ in range(3):
-            fn(stream)
-        times = []
-        with torch.cuda.stream(stream):
-            for _ in range(iters):
-                flush_l2(torch, scratch)
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                fn(stream)
-                b.record(stream)
-                b.synchronize()
-                times.append(a.elapsed_time(b) * 1e3)
-        us = statistics.median(times)
+        us = flushed_median_us(torch, stream, scratch, lambda: fn(stream), iters)
         nbytes = collective_bytes(kind, N, count, 2, 128)
         out[kind] = {"us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
                      "bytes_alg": nbytes, "count_per_rank": count, "l2": "flushed"}
@@ -527,20 +521,7 @@ def measure_staged(torch, stream, iters=10):
         }
         row = {}
         for kind, fn in calls.items():
-            for _ in range(3):
-                fn()
-            times = []
-            with torch.cuda.stream(stream):
-                for _ in range(iters):
-                    flush_l2(torch, scratch)
-                    a = torch.cuda.Event(enable_timing=True)
-                    b = torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    fn()
-                    b.record(stream)
-                    b.synchronize()
-                    times.append(a.elapsed_time(b) * 1e3)
-            us = statistics.median(times)
+            us = flushed_median_us(torch, stream, scratch, fn, iters)
             nbytes = staged_bytes(kind, N, n, w.elem_bytes)
             row[kind] = {"us": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                          "bytes_alg": nbytes}
@@ -582,22 +563,12 @@ def measure_variants(torch, stream, n=1 << 22, iters=10):
                 step()
             torch.cuda.synchronize()
             err = out.double() - exact
-            times = []
-            with torch.cuda.stream(stream):
-                for _ in range(iters):
-                    flush_l2(torch, scratch)
-                    a = torch.cuda.Event(enable_timing=True)
-                    b = torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    step()
-                    b.record(stream)
-                    b.synchronize()
-                    times.append(a.elapsed_time(b) * 1e3)
+            us = flushed_median_us(torch, stream, scratch, step, iters, warmup=0)
             res["%s/%d" % (fname, block)] = {
                 "rel_l2_error": float(torch.linalg.vector_norm(err)) / norm,
                 "max_abs_error_over_max": float(err.abs().max()) / peak,
                 "compression": round(4 / (1 + 4 / block), 4),
-                "us_staged": round(statistics.median(times), 2)}
+                "us_staged": round(us, 2)}
     del ins, exact, out, codes, scales, scratch
     torch.cuda.empty_cache()
     return res
@@ -739,21 +710,10 @@ def run_crossover(args):
             bufs.load(W.random_inputs(N, n, W.BF16, 5, scale_spread=1.0))
             s = stream.cuda_stream
             for algo in ("flat", "tree"):
-                for _ in range(3):
-                    bufs.run(algo, s)
-                times = []
-                with torch.cuda.stream(stream):
-                    for _ in range(args.steps):
-                        flush_l2(torch, scratch)
-                        a = torch.cuda.Event(enable_timing=True)
-                        b = torch.cuda.Event(enable_timing=True)
-                        a.record(stream)
-                        bufs.run(algo, s)
-                        b.record(stream)
-                        b.synchronize()
-                        times.append(a.elapsed_time(b) * 1e3)
+                us = flushed_median_us(torch, stream, scratch,
+                                       lambda: bufs.run(algo, s), args.steps)
                 key = "%s_%s_us" % ("lp" if block else "exact", algo)
-                row[key] = round(statistics.median(times), 3)
+                row[key] = round(us, 3)
             del bufs
             torch.cuda.empty_cache()
         print(json.dumps(row), flush=True)
