@@ -2,7 +2,6 @@
 bit for bit, through the C ABI: both dtypes, exact and low precision, rank
 counts 1..16, ragged sizes and lengths that are not a multiple of 16 bytes
 (element-wise path). Output buffers carry guard bands."""
-import numpy as np
 import pytest
 import torch
 

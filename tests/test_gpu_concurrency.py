@@ -6,7 +6,6 @@ import threading
 import pytest
 import torch
 
-import precision_collective_reduction_gb300 as pcr
 from precision_collective_reduction_gb300 import runner, workloads as W
 
 pytestmark = pytest.mark.gpu

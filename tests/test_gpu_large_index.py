@@ -5,7 +5,6 @@ kernels is 64-bit. Two ranks of 2^31 + 200 FP32 elements (8.6 GB each, about
 are checked against the oracle. The inputs are drawn on the GPU by PyTorch's
 seeded generator (not by this library) and the sampled blocks are copied to
 the host for the oracle."""
-import numpy as np
 import pytest
 import torch
 

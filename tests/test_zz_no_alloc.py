@@ -10,7 +10,6 @@ first failure has already run every other test.
 """
 import ctypes
 
-import numpy as np
 import pytest
 
 from precision_collective_reduction_gb300 import _binding as B
