@@ -282,7 +282,8 @@ def _error_bound_ok(x, back, scales, n):
 
 
 def pin_error_bound(oracle):
-    n = 128 * 64 + 37
+    # 10^7 values per distribution (plus a ragged tail block)
+    n = 10 ** 7 + 37
     g = np.random.default_rng(5)
     cases = [
         g.standard_normal(n).astype(np.float32),
@@ -462,31 +463,49 @@ def pin_exact_tree_equals_flat(oracle):
                 assert same_bits(a, b)
 
 
+def _wire_sum(wc, ws, n):
+    """The rank-ordered binary32 sum S of the dequantized wire payloads,
+    from PyTorch's E4M3 decoding and numpy binary32 arithmetic (one rounded
+    multiply per element, then one rounded add per rank)."""
+    table = torch_e4m3_table()
+    S = None
+    for c, s in zip(wc, ws):
+        v = (table[c] * np.repeat(s, 128)[:n]).astype(np.float32)
+        S = v if S is None else (S + v).astype(np.float32)
+    return S
+
+
 def pin_tree_requant_grid(oracle):
-    # FP32 flat outputs are the fixed-order sums S themselves. The tree's
-    # shard payload must be S requantized on its own block scale: the scale
-    # is max|S|/448 (numpy IEEE division), the codes are PyTorch's encoding
-    # of S * (448/max|S|), and every output is within one half-spacing of S.
-    ins = W.random_inputs(4, 128 * 9 + 50, F32, 91, scale_spread=2.0)
-    S = oracle.flat(ins)[0][0]
-    outs, _, _, sc, ss = oracle.tree(ins)
-    n = S.size
-    for b in range(ss.size):
-        blk = S[b * 128:(b + 1) * 128]
-        a = np.float32(np.max(np.abs(blk)))
-        assert ss[b] == a / np.float32(448.0), b
-        inv = np.float32(448.0) / a
-        assert np.array_equal(sc[b * 128:(b + 1) * 128],
-                              torch_e4m3_encode((blk * inv).astype(np.float32))), b
-    # outputs lie on the requantized grid: PyTorch's decode of the shard code
-    # times the shard scale (one numpy binary32 multiply)
-    grid = (torch_e4m3_table()[sc] * np.repeat(ss, 128)[:n]).astype(np.float32)
-    for o in outs:
-        assert same_bits(o, grid)
-    assert np.count_nonzero(outs[0] != S) > n // 2
-    s = np.repeat(ss.astype(np.float64), 128)[:n]
-    err = np.abs(outs[0].astype(np.float64) - S.astype(np.float64))
-    assert np.all(err <= 2.0 ** -4 * np.abs(S) + 2.0 ** -10 * s * (1 + 2.0 ** -20))
+    # The tree requantizes the binary32 sum S of the dequantized payloads
+    # (for BF16 data too: the sum is cast to BF16 only at the output). Its
+    # shard scale must be max|S|/448 (numpy IEEE division), its codes
+    # PyTorch's encoding of S * (448/max|S|), and every output the cast of
+    # PyTorch's decode of the shard code times the shard scale.
+    for dt in (F32, BF16):
+        ins = W.random_inputs(4, 128 * 9 + 50, dt, 91, scale_spread=2.0)
+        n = ins[0].size
+        outs, wc, ws, sc, ss = oracle.tree(ins)
+        for r, x in enumerate(ins):  # the published payloads are each rank's own
+            c, s = oracle.quantize(x)
+            assert np.array_equal(wc[r], c) and same_bits(ws[r], s), (dt, r)
+        S = _wire_sum(wc, ws, n)
+        flat0 = oracle.flat(ins)[0][0]
+        assert same_bits(flat0, S if dt == F32 else torch_bf16_bits(S)), dt
+        for b in range(ss.size):
+            blk = S[b * 128:(b + 1) * 128]
+            a = np.float32(np.max(np.abs(blk)))
+            assert ss[b] == a / np.float32(448.0), (dt, b)
+            inv = np.float32(448.0) / a
+            assert np.array_equal(sc[b * 128:(b + 1) * 128],
+                                  torch_e4m3_encode((blk * inv).astype(np.float32))), (dt, b)
+        grid = (torch_e4m3_table()[sc] * np.repeat(ss, 128)[:n]).astype(np.float32)
+        want = grid if dt == F32 else torch_bf16_bits(grid)
+        for o in outs:
+            assert same_bits(o, want), dt
+        assert np.count_nonzero(grid != S) > n // 2
+        s = np.repeat(ss.astype(np.float64), 128)[:n]
+        err = np.abs(grid.astype(np.float64) - S.astype(np.float64))
+        assert np.all(err <= 2.0 ** -4 * np.abs(S) + 2.0 ** -10 * s * (1 + 2.0 ** -20))
 
 
 def pin_torch_full_example(oracle):
@@ -505,6 +524,28 @@ def pin_torch_full_example(oracle):
                 assert np.all(ws[r] == np.float32(r) / np.float32(448.0)), r
                 assert np.all(np.abs(widen(outs[r]) - T) <= bound)
                 assert same_bits(outs[r], outs[0])
+            # Closed form of the low-precision results. Rank r's blocks hold
+            # the constant r, so their scale is fl(r/448) and every code is
+            # 448 (rank 0: a zero block, scale 0, code +0): rank r decodes to
+            # v_r = fl(448 * fl(r/448)) and S is the rank-ordered binary32
+            # sum of the v_r. Tree: S is constant in every block, so the
+            # shard codes are 448 with scale fl(S/448) and every output is
+            # the cast of fl(448 * fl(S/448)).
+            f = np.float32
+            S = f(0.0)
+            for r in range(1, N):
+                S = f(S + f(f(448.0) * f(f(r) / f(448.0))))
+
+            def cast(v):
+                full = np.full(rows * cols, v, dtype=np.float32)
+                return torch_bf16_bits(full) if ins[0].dtype == np.uint16 else full
+            for o in outs:
+                assert same_bits(o, cast(S)), (N, "flat")
+            touts, twc, tws, sc, ss = oracle.tree(ins)
+            assert np.all(sc == (0x7E if S > 0 else 0x00)), (N, "tree codes")
+            assert np.all(ss == f(S / f(448.0))), (N, "tree scales")
+            for o in touts:
+                assert same_bits(o, cast(f(f(448.0) * f(S / f(448.0))))), (N, "tree")
 
 
 def pin_compression(oracle):

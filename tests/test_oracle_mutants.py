@@ -71,6 +71,9 @@ MUTANTS = [
     ("fmt_reduce_reversed",
      "        float sum = dequant_elem_fmt(codes[0], scales[0], block, i, fmt);\n        for (r = 1; r < nranks; r++)\n            sum = sum + dequant_elem_fmt(codes[r], scales[r], block, i, fmt);",
      "        float sum = dequant_elem_fmt(codes[nranks - 1], scales[nranks - 1], block, i, fmt);\n        for (r = nranks - 2; r >= 0; r--)\n            sum = sum + dequant_elem_fmt(codes[r], scales[r], block, i, fmt);"),
+    ("tree_requant_bf16_sum",
+     "                sum = sum + dequant_elem(wire_codes[r], wire_scales[r], block, i);\n            reduced[i] = sum;",
+     "                sum = sum + dequant_elem(wire_codes[r], wire_scales[r], block, i);\n            reduced[i] = dtype == ORC_BF16 ? orc_bf16_to_f32(orc_f32_to_bf16(sum)) : sum;"),
     ("a2a_global_blocks",
      "                st = orc_quantize(elem_ptr(in[r], dtype, (size_t)j * c), dtype, c, block,\n                                  wire_codes[r] + (size_t)j * c,\n                                  wire_scales[r] + (size_t)j * nbc);",
      "                st = j ? 0 : orc_quantize(in[r], dtype, c * (size_t)nranks, block,\n                                          wire_codes[r], wire_scales[r]);"),
