@@ -69,6 +69,8 @@ def _load(path):
                                  ctypes.c_int, vp, ctypes.c_int]
     for f in ("orc_quantize_fmt", "orc_dequantize_fmt", "orc_reduce_fmt"):
         getattr(L, f).restype = ctypes.c_int
+    L.orc_set_divide_reading.argtypes = [ctypes.c_int]
+    L.orc_set_divide_reading.restype = None
     L.orc_shard_len.argtypes = [c_sz, ctypes.c_int, ctypes.c_int]
     L.orc_shard_len.restype = c_sz
     for f in ("orc_quantize", "orc_dequantize", "orc_reduce", "orc_flat",
@@ -95,6 +97,19 @@ def using(path):
         yield
     finally:
         _lib = saved
+
+
+@contextlib.contextmanager
+def divide_reading():
+    """Inside the block, quantize elements as fp8(x / s) (one division per
+    element) instead of fp8(x * (448 / a)): the other reading of the scale
+    step, for comparing the two readings only."""
+    L = lib()
+    L.orc_set_divide_reading(1)
+    try:
+        yield
+    finally:
+        L.orc_set_divide_reading(0)
 
 
 def _ptr(a):

@@ -251,6 +251,17 @@ void orc_block_scale(float amax, float *s, float *inv)
     orc_block_scale_fmt(amax, ORC_E4M3, s, inv);
 }
 
+/* The other reading of the scale step, off by default: elements encoded as
+ * fp8(x / s), one IEEE division per element, instead of fp8(x * inv). The
+ * pages fix neither; this switch exists only to count how often the two
+ * readings give different codes, and nothing in the default path uses it. */
+static int g_divide_reading = 0;
+
+void orc_set_divide_reading(int on)
+{
+    g_divide_reading = on != 0;
+}
+
 /* Quantize values v[0..len) (one block) into codes[0..len) and return s. */
 static float quantize_block_fmt(const float *v, size_t len, uint8_t *codes, int fmt)
 {
@@ -264,6 +275,8 @@ static float quantize_block_fmt(const float *v, size_t len, uint8_t *codes, int 
             codes[i] = signbit(v[i]) ? 0x80 : 0x00;
         } else {
             float y = v[i] * inv;
+            if (g_divide_reading)
+                y = v[i] / s;
             codes[i] = fp8_encode(fmt, y);
         }
     }
