@@ -151,7 +151,8 @@ def profiled_traffic(kernel_key):
 
 
 class ClockSampler:
-    """nvidia-smi SM clock / throttle-reason samples every 100 ms."""
+    """nvidia-smi SM clock / throttle-reason samples every 100 ms, from
+    construction to stop()."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -184,15 +185,18 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, t0, t1):
+    def summary(self, t0, t1, widen=True):
+        """Median SM clock, its maximum and the throttle reasons seen in the
+        samples taken between t0 and t1 (window "timed"); with widen, a
+        window of fewer than 3 samples is widened to all samples ("run")."""
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
         inside = [p for t, p in self.samples if t0 <= t <= t1]
-        window = "timed"
-        if len(inside) < 3:  # short timed region: widen to the whole GPU phase
+        window = "timed" if widen else "gpu phase"
+        if widen and len(inside) < 3:
             inside = [p for _, p in self.samples]
             window = "run"
         if not inside:
@@ -520,15 +524,99 @@ def measure_staged(torch, stream, iters=10):
             "lp_reduce": lambda: pcr.lp_reduce(codes, scales, out, stream=stream),
         }
         row = {}
+        small = w.nranks * w.message_bytes < L2_FLUSH_BYTES
         for kind, fn in calls.items():
             us = flushed_median_us(torch, stream, scratch, fn, iters)
             nbytes = staged_bytes(kind, N, n, w.elem_bytes)
             row[kind] = {"us": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                          "bytes_alg": nbytes}
+            if small:
+                # per call without launch gaps: back to back, and replayed
+                # from a CUDA graph (both warm: one rank's message fits L2)
+                row[kind]["warm_us_per_call"] = round(back_to_back_us(torch, stream, fn, 200), 2)
+                row[kind]["graph_us_per_call"] = round(graph_us(torch, stream, fn, 100), 2)
+        if small:
+            row["chain"] = measure_staged_chain(torch, stream, scratch, ins, codes, scales, out,
+                                                iters)
         res[w.name] = row
         del ins, codes, scales, out
         torch.cuda.empty_cache()
     del scratch
+    return res
+
+
+def back_to_back_us(torch, stream, fn, calls):
+    """us per call of `calls` calls of fn() enqueued back to back on stream."""
+    with torch.cuda.stream(stream):
+        fn()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(calls):
+            fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / calls
+
+
+def graph_us(torch, stream, fn, calls):
+    """us per call of fn() captured `calls` times into one CUDA graph on
+    stream and replayed (median of 5 replays)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    t = []
+    for _ in range(5):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        t.append(a.elapsed_time(b) * 1e3 / calls)
+    del g
+    return statistics.median(t)
+
+
+def measure_staged_chain(torch, stream, scratch, ins, codes, scales, out, iters):
+    """The staged allreduce of N ranks (lp_quantize of every rank's message,
+    then lp_reduce of the N payloads): L2-flushed single chains, and per
+    chain from a CUDA graph of back-to-back chains, with the N quantize calls
+    on the one stream (each waits for the previous kernel) or on N parallel
+    graph branches (one stream per rank, as the N ranks quantize at once)."""
+    import precision_collective_reduction_gb300 as pcr
+    N, n = len(ins), ins[0].numel()
+    branches = [torch.cuda.Stream() for _ in range(N)]
+
+    def serial():
+        for r in range(N):
+            pcr.lp_quantize(ins[r], codes[r], scales[r], stream=stream)
+        pcr.lp_reduce(codes, scales, out, stream=stream)
+
+    def branched():
+        for r in range(N):
+            branches[r].wait_stream(stream)
+            pcr.lp_quantize(ins[r], codes[r], scales[r], stream=branches[r])
+        for r in range(N):
+            stream.wait_stream(branches[r])
+        pcr.lp_reduce(codes, scales, out, stream=stream)
+
+    elem = ins[0].element_size()
+    nbytes = N * staged_bytes("lp_quantize", N, n, elem) + staged_bytes("lp_reduce", N, n, elem)
+    peak, _ = measured_peaks()
+    res = {"bytes_alg": nbytes,
+           "note": "%d x lp_quantize + lp_reduce; bytes: every quantize's input read and "
+                   "payload written, the reduce's %d payloads read and output written" % (N, N)}
+    for name, fn in (("serial", serial), ("branched", branched)):
+        us = flushed_median_us(torch, stream, scratch, fn, iters)
+        gus = graph_us(torch, stream, fn, 20)
+        res[name] = {"us": round(us, 2), "graph_us_per_call": round(gus, 2),
+                     "graph_GBps": round(nbytes / gus / 1e3, 1),
+                     "graph_frac_of_peak": round(nbytes / gus / 1e3 / peak, 4)}
     return res
 
 
@@ -601,11 +689,12 @@ def run_ours(args):
     bufs.load(host)
     torch.cuda.synchronize()
 
+    # sampled through every GPU leg below; summarized for the timed steps
+    # and for the whole GPU phase
     clocks = ClockSampler(local)
+    phase_t0 = time.monotonic()
     total_ms, per_kernel, (t0, t1) = timed_steps(torch, bufs, w, stream, args.steps,
                                                  args.warmup, dist)
-    clocks.stop()  # samples are needed for the timed region only
-    clock_info = clocks.summary(t0, t1)
     total_ms = max_over_ranks(total_ms, dist, "cuda")
     sbytes = step_bytes(w)
     value = whole_job_gbps(sbytes, args.steps, world, total_ms)
@@ -667,6 +756,10 @@ def run_ours(args):
         extras["ablation_fp8_block"] = measure_variants(torch, stream)
         extras["staged"] = measure_staged(torch, stream)
 
+    clocks.stop()
+    clock_info = clocks.summary(t0, t1)
+    clock_phase = clocks.summary(phase_t0, time.monotonic(), widen=False)
+
     if rank != 0:
         return 0
     line = {
@@ -680,7 +773,7 @@ def run_ours(args):
         "hbm_frac_nominal": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": roofline, "kernels": kernels,
         "e2e": e2e, "gpu_launches": len(w.algos) * args.steps,
-        "clocks": clock_info,
+        "clocks": clock_info, "clocks_gpu_phase": clock_phase,
     }
     line.update(extras)
     if world == 1 and not args.no_cpu_baseline:
@@ -702,7 +795,7 @@ def run_crossover(args):
     stream = torch.cuda.Stream()
     scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     N = 8
-    for kib in (8, 32, 128, 512, 2048, 8192, 32768, 131072):
+    for kib in (8, 32, 128, 512, 2048, 8192, 32768, 131072, 262144):
         n = kib * 1024 // 2
         row = {"nranks": N, "message_KiB": kib, "dtype": "bf16"}
         for block in (0, 128):

@@ -41,12 +41,13 @@
  *     while the previous kernel of the stream still runs, but it touches no
  *     memory before that kernel has completed, so stream order holds for
  *     every buffer, also inside CUDA graph capture.
- *   - Resources: kernels of 256 threads, grids of at most 4 CTAs per SM.
- *     FP32 low-precision allreduces of 8 ranks with 1 GiB of input or more,
- *     and low-precision all-gathers of 16-byte-aligned contributions, stage
- *     results in up to 46 KB of dynamic shared memory per CTA and write
- *     them with bulk (TMA) copies; every copy has completed when the
- *     kernel does.
+ *   - Resources: kernels of 256 threads, one warp per work item (grids
+ *     grow with the message and may exceed what the GPU holds at once; no
+ *     CTA ever waits on another). FP32 low-precision allreduces of 8 ranks
+ *     with 1 GiB of input or more, and low-precision all-gathers of
+ *     16-byte-aligned contributions, stage results in up to 46 KB of
+ *     dynamic shared memory per CTA and write them with bulk (TMA) copies;
+ *     every copy has completed when the kernel does.
  *   - Return value: LPCOLL_OK, or an lpcoll_status error found before any
  *     launch (nothing is enqueued then), or LPCOLL_ERR_CUDA if the launch
  *     itself failed (lpcoll_last_cuda_error() gives the cudaError_t).
@@ -242,7 +243,10 @@ int all_to_all_sim(const void *const *in, void *const *out, int nranks,
  * copy_out_stream). Errors: LPCOLL_ERR_ARG (dtype, nranks, slots, chunk,
  * workspace NULL or too small, no output), LPCOLL_ERR_UNSUPPORTED (block),
  * LPCOLL_ERR_RANK (NULL per-rank pointer), LPCOLL_ERR_ALIGN (workspace),
- * LPCOLL_ERR_CUDA (a copy, launch or event failed).                       */
+ * LPCOLL_ERR_CUDA (a copy, launch or event failed). After LPCOLL_ERR_CUDA
+ * the call has still waited for all three streams, so nothing it queued
+ * reads host_in or writes the outputs or the workspace any more: the caller
+ * may free or reuse them at once (the outputs' contents are undefined).   */
 size_t lpcoll_host_workspace_bytes(int nranks, size_t chunk, lpcoll_dtype dtype,
                                    int block, int flat, int tree, int slots);
 int lpcoll_host_allreduce(const void *const *host_in, void *const *host_out_flat,
@@ -251,6 +255,17 @@ int lpcoll_host_allreduce(const void *const *host_in, void *const *host_out_flat
                           void *workspace, size_t workspace_bytes,
                           void *copy_in_stream, void *compute_stream,
                           void *copy_out_stream);
+
+/* Test hook for the error path of lpcoll_host_allreduce; not part of the
+ * method. The next call of lpcoll_host_allreduce that passes its argument
+ * checks treats its enqueue step number `step` (0 = the first copy, event
+ * record or wait, or launch it would queue, in queue order) as failed
+ * without calling CUDA for it: the steps before it are queued as usual, none
+ * after it, and the call returns LPCOLL_ERR_CUDA with
+ * lpcoll_last_cuda_error() == cudaErrorInvalidValue. The hook then disarms
+ * itself; a negative step disarms it at once. It lets a test drive the
+ * error return with no failing GPU call.                                   */
+void lpcoll_debug_fail_host_enqueue(long step);
 
 /* dda_flat_sim with block = 128 for callers that cannot allocate device
  * memory. The pages have no counterpart: this exists for users of the
@@ -270,8 +285,10 @@ int lpcoll_host_allreduce(const void *const *host_in, void *const *host_out_flat
  *   memory   every GPU on which the library's kernels are loaded holds the
  *            array (about 66 MiB) until the process exits. The first call
  *            with a device current looks up the array's device address on
- *            that device (cudaGetSymbolAddress); make that first call before
- *            any stream capture.
+ *            that device (cudaGetSymbolAddress) and keeps it for the life
+ *            of the process; make that first call before any stream capture,
+ *            and do not use this call across a device reset
+ *            (cudaDeviceReset), after which the kept address is stale.
  *   sharing  all calls share the one array and it keeps the last call's
  *            wire payload (nothing in it needs to start at zero). Calls that
  *            overlap on the GPU (different streams, or threads) race on it:
@@ -280,6 +297,32 @@ int lpcoll_host_allreduce(const void *const *host_in, void *const *host_out_flat
 #define LPCOLL_NOALLOC_MAX_ELEMS (64u * 1024u * 1024u)
 int dda_flat_sim_noalloc(const void *const *in, void *const *out, int nranks,
                          size_t n, lpcoll_dtype dtype, void *stream);
+
+/* Bounds checks, a test tool with no counterpart in the method. The
+ * bounds-checked build of this library (liblpcoll_debug_bounds.so, compiled
+ * with -DLPCOLL_DEBUG_BOUNDS) makes every entry point list the buffers its
+ * call may touch, with the sizes this header gives them (inputs read-only;
+ * outputs, wires and workspaces writable), and checks every global load,
+ * store and bulk copy of its kernels against that list before the access.
+ * An access outside the list is skipped (a skipped load reads zeros) and
+ * recorded; nothing traps, so the CUDA context stays usable. That build
+ * allocates one small managed record on first use, copies the buffer list
+ * to the device ahead of every launch (so its calls are slower and must
+ * not be captured into a CUDA graph), and is for tests only.
+ *
+ * lpcoll_debug_bounds_errors waits for the device (cudaDeviceSynchronize)
+ * and returns 1 if any access failed its check since the previous call
+ * (*first_bad, when first_bad is not NULL, receives the first such
+ * address), 0 if none, -2 if the device or the record failed; it then
+ * clears the record. The normal build returns -1 and checks nothing.
+ *
+ * lpcoll_debug_bounds_shrink(bytes) makes the next call of the
+ * bounds-checked build list every buffer `bytes` shorter than its real
+ * size, so that the kernels' last legitimate accesses fail the check (and
+ * are skipped): it shows the checks fire without any access leaving the
+ * real buffers. The normal build ignores it.                              */
+int lpcoll_debug_bounds_errors(unsigned long long *first_bad);
+void lpcoll_debug_bounds_shrink(size_t bytes);
 
 /* Static, NUL-terminated name of a status code (never NULL). */
 const char *lpcoll_status_string(int status);

@@ -7,6 +7,7 @@ of the same name, and raises ``LpcollError`` on a non-zero status. All the
 arithmetic runs in the library's kernels. There is no fallback: if the
 library is missing, every call raises.
 """
+import contextlib
 import ctypes
 import os
 
@@ -42,35 +43,68 @@ def lib():
             raise RuntimeError(
                 "liblpcoll.so not found at %s; build it with "
                 "precision_collective_reduction_gb300.build.build()" % LIB_PATH)
-        L = ctypes.CDLL(LIB_PATH)
-        vp, sz, ci = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
-        pp = ctypes.POINTER(ctypes.c_void_p)
-        L.lp_quantize.argtypes = [vp, ci, sz, ci, vp, vp, vp]
-        L.lp_dequantize.argtypes = [vp, vp, sz, ci, vp, ci, vp]
-        L.lp_reduce.argtypes = [pp, pp, ci, sz, ci, vp, ci, vp]
-        L.dda_flat_sim.argtypes = [pp, pp, ci, sz, ci, ci, pp, pp, vp]
-        L.dda_tree_sim.argtypes = [pp, pp, ci, sz, ci, ci, pp, pp, vp, vp, vp]
-        for f in ("reduce_scatter_sim", "all_gather_sim", "all_to_all_sim"):
-            getattr(L, f).argtypes = [pp, pp, ci, sz, ci, ci, pp, pp, vp]
-        L.dda_flat_sim_noalloc.argtypes = [pp, pp, ci, sz, ci, vp]
-        L.lp_quantize_fmt.argtypes = [vp, ci, sz, ci, ci, vp, vp, vp]
-        L.lp_dequantize_fmt.argtypes = [vp, vp, sz, ci, ci, vp, ci, vp]
-        L.lp_reduce_fmt.argtypes = [pp, pp, ci, sz, ci, ci, vp, ci, vp]
-        L.lpcoll_host_workspace_bytes.argtypes = [ci, sz, ci, ci, ci, ci, ci]
-        L.lpcoll_host_workspace_bytes.restype = sz
-        L.lpcoll_host_allreduce.argtypes = [pp, pp, pp, ci, sz, ci, ci, sz, ci, vp, sz,
-                                            vp, vp, vp]
-        L.lpcoll_host_allreduce.restype = ci
-        for f in ("lp_quantize", "lp_dequantize", "lp_reduce", "dda_flat_sim",
-                  "dda_tree_sim", "reduce_scatter_sim", "all_gather_sim",
-                  "all_to_all_sim", "dda_flat_sim_noalloc", "lp_quantize_fmt",
-                  "lp_dequantize_fmt", "lp_reduce_fmt",
-                  "lpcoll_last_cuda_error", "lpcoll_version"):
-            getattr(L, f).restype = ci
-        L.lpcoll_status_string.argtypes = [ci]
-        L.lpcoll_status_string.restype = ctypes.c_char_p
-        _lib = L
+        _lib = _load(LIB_PATH)
     return _lib
+
+
+@contextlib.contextmanager
+def using_library(path):
+    """Route every call of this module through another build of the library
+    inside the block (the tests use the bounds-checked build this way)."""
+    global _lib
+    saved = _lib
+    _lib = _load(path)
+    try:
+        yield _lib
+    finally:
+        _lib = saved
+
+
+def _load(path):
+    """Load one build of the library and declare its C signatures."""
+    L = ctypes.CDLL(path)
+    vp, sz, ci = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    L.lp_quantize.argtypes = [vp, ci, sz, ci, vp, vp, vp]
+    L.lp_dequantize.argtypes = [vp, vp, sz, ci, vp, ci, vp]
+    L.lp_reduce.argtypes = [pp, pp, ci, sz, ci, vp, ci, vp]
+    L.dda_flat_sim.argtypes = [pp, pp, ci, sz, ci, ci, pp, pp, vp]
+    L.dda_tree_sim.argtypes = [pp, pp, ci, sz, ci, ci, pp, pp, vp, vp, vp]
+    for f in ("reduce_scatter_sim", "all_gather_sim", "all_to_all_sim"):
+        getattr(L, f).argtypes = [pp, pp, ci, sz, ci, ci, pp, pp, vp]
+    L.dda_flat_sim_noalloc.argtypes = [pp, pp, ci, sz, ci, vp]
+    L.lp_quantize_fmt.argtypes = [vp, ci, sz, ci, ci, vp, vp, vp]
+    L.lp_dequantize_fmt.argtypes = [vp, vp, sz, ci, ci, vp, ci, vp]
+    L.lp_reduce_fmt.argtypes = [pp, pp, ci, sz, ci, ci, vp, ci, vp]
+    L.lpcoll_host_workspace_bytes.argtypes = [ci, sz, ci, ci, ci, ci, ci]
+    L.lpcoll_host_workspace_bytes.restype = sz
+    L.lpcoll_host_allreduce.argtypes = [pp, pp, pp, ci, sz, ci, ci, sz, ci, vp, sz,
+                                        vp, vp, vp]
+    L.lpcoll_host_allreduce.restype = ci
+    L.lpcoll_debug_fail_host_enqueue.argtypes = [ctypes.c_long]
+    L.lpcoll_debug_fail_host_enqueue.restype = None
+    for f in ("lp_quantize", "lp_dequantize", "lp_reduce", "dda_flat_sim",
+              "dda_tree_sim", "reduce_scatter_sim", "all_gather_sim",
+              "all_to_all_sim", "dda_flat_sim_noalloc", "lp_quantize_fmt",
+              "lp_dequantize_fmt", "lp_reduce_fmt",
+              "lpcoll_last_cuda_error", "lpcoll_version"):
+        getattr(L, f).restype = ci
+    L.lpcoll_status_string.argtypes = [ci]
+    L.lpcoll_status_string.restype = ctypes.c_char_p
+    L.lpcoll_debug_bounds_errors.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
+    L.lpcoll_debug_bounds_errors.restype = ci
+    L.lpcoll_debug_bounds_shrink.argtypes = [sz]
+    L.lpcoll_debug_bounds_shrink.restype = None
+    return L
+
+
+def debug_bounds_errors():
+    """(status, first bad address) of the bounds-checked build: status 1 if
+    a kernel access since the last call fell outside the buffers its call
+    passed, 0 if none, -1 for the normal build. Synchronizes the device."""
+    bad = ctypes.c_ulonglong(0)
+    st = lib().lpcoll_debug_bounds_errors(ctypes.byref(bad))
+    return st, bad.value
 
 
 def status_string(status):

@@ -18,7 +18,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblpcoll.so")
-STAMP = os.path.join(BUILD, "stamp")
+# The bounds-checked build (-DLPCOLL_DEBUG_BOUNDS): every global access of the
+# kernels is checked against the buffers its call passed; for tests only.
+DEBUG_BUILD = os.path.join(BUILD, "debug_bounds")
+DEBUG_LIB = os.path.join(PKG, "liblpcoll_debug_bounds.so")
 
 SOURCES = ["lpcoll_api.cu", "lpcoll_codec.cu", "lpcoll_dda_f32.cu",
            "lpcoll_dda_bf16.cu", "lpcoll_scatter_f32.cu", "lpcoll_scatter_bf16.cu",
@@ -55,19 +58,23 @@ def _digest(extra):
     return h.hexdigest()
 
 
-def build(force: bool = False, extra_flags=()) -> str:
-    """Compile and link liblpcoll.so; returns its path."""
-    flags = NVCC_FLAGS + list(extra_flags)
+def build(force: bool = False, extra_flags=(), debug_bounds: bool = False) -> str:
+    """Compile and link liblpcoll.so (debug_bounds: the bounds-checked
+    liblpcoll_debug_bounds.so); returns its path."""
+    flags = NVCC_FLAGS + list(extra_flags) + (["-DLPCOLL_DEBUG_BOUNDS"] if debug_bounds else [])
+    build_dir = DEBUG_BUILD if debug_bounds else BUILD
+    lib = DEBUG_LIB if debug_bounds else LIB
+    stamp = os.path.join(build_dir, "stamp")
     digest = _digest(flags)
-    if not force and os.path.exists(LIB) and os.path.exists(STAMP):
-        with open(STAMP) as f:
+    if not force and os.path.exists(lib) and os.path.exists(stamp):
+        with open(stamp) as f:
             if f.read().strip() == digest:
-                return LIB
-    os.makedirs(BUILD, exist_ok=True)
+                return lib
+    os.makedirs(build_dir, exist_ok=True)
     exe = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [exe, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -76,16 +83,25 @@ def build(force: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     cmd = [exe, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    with open(STAMP, "w") as f:
+    os.replace(tmp, lib)
+    with open(stamp, "w") as f:
         f.write(digest)
-    return LIB
+    return lib
+
+
+def build_all(force: bool = False) -> str:
+    """Both libraries, compiled at once; returns the path of liblpcoll.so."""
+    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+        main = ex.submit(build, force)
+        dbg = ex.submit(build, force, (), True)
+        dbg.result()
+        return main.result()
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv))
+    print(build_all(force="--force" in sys.argv))

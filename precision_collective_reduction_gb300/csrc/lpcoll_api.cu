@@ -1,14 +1,15 @@
 // lpcoll_api.cu -- the extern "C" entry points of liblpcoll.so: argument
-// checks (all done on the host before anything is enqueued), launch sizing,
-// and dispatch to the kernels. The semantics of each call are documented in
+// checks (all done on the host before anything is enqueued) and dispatch to
+// the kernels. The semantics of each call are documented in
 // include/lpcoll.h.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <initializer_list>
+#ifdef LPCOLL_DEBUG_BOUNDS
+#include <atomic>
 #include <mutex>
-#include <unordered_map>
-#include <utility>
+#endif
 
 #include "lpcoll.h"
 #include "lpcoll_dda.cuh"
@@ -36,62 +37,6 @@ cudaError_t launch_all_to_all(const DdaParams &p, int nranks, size_t c, int dtyp
 namespace {
 
 thread_local int g_last_cuda_error = 0;
-
-struct OccKey {
-    const void *fn;
-    int dev;
-    size_t smem;
-    bool operator==(const OccKey &o) const
-    {
-        return fn == o.fn && dev == o.dev && smem == o.smem;
-    }
-};
-struct OccHash {
-    size_t operator()(const OccKey &k) const
-    {
-        return std::hash<const void *>()(k.fn) ^ (static_cast<size_t>(k.dev) << 1) ^
-               (k.smem << 7);
-    }
-};
-
-std::mutex g_occ_mutex;
-// SM count and resident CTAs per SM of each kernel on each device
-std::unordered_map<OccKey, std::pair<int, int>, OccHash> g_wave;
-
-// SM count and resident CTAs per SM of kernel (0, 0 if the queries fail).
-std::pair<int, int> occupancy(const void *kernel, size_t smem)
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return {0, 0};
-    }
-    std::lock_guard<std::mutex> lock(g_occ_mutex);
-    auto it = g_wave.find(OccKey{kernel, dev, smem});
-    if (it != g_wave.end())
-        return it->second;
-    int sms = 0, per_sm = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) !=
-            cudaSuccess) {
-        // not cached, and no error left behind
-        cudaGetLastError();
-        return {0, 0};
-    }
-    g_wave.emplace(OccKey{kernel, dev, smem}, std::make_pair(sms, per_sm));
-    return {sms, per_sm};
-}
-
-int full_wave(const void *kernel, int cap, size_t smem)
-{
-    const std::pair<int, int> occ = occupancy(kernel, smem);
-    const int sms = occ.first;
-    int per_sm = occ.second;
-    if (per_sm > cap)
-        per_sm = cap;
-    const int wave = sms * per_sm;
-    return wave < 1 ? 1 : wave;
-}
 
 inline bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
@@ -143,6 +88,32 @@ int first_error(std::initializer_list<int> sts)
     return align;
 }
 
+size_t elem_bytes(int dtype) { return dtype == LPCOLL_F32 ? 4 : 2; }
+
+size_t blocks_of(size_t n, int block) { return (n + block - 1) / block; }
+
+// Bounds-checked build: the buffers of an allreduce-shaped call (inputs read,
+// outputs and wires written, and the tree's shard payload when given).
+void debug_dda_ranges(const void *const *in, void *const *out, int nranks, size_t n,
+                      int dtype, int block, uint8_t *const *wire_codes,
+                      float *const *wire_scales, const uint8_t *shard_codes,
+                      const float *shard_scales)
+{
+    debug_begin();
+    for (int r = 0; r < nranks; ++r) {
+        debug_range(in[r], n * elem_bytes(dtype), false);
+        debug_range(out[r], n * elem_bytes(dtype), true);
+        if (block) {
+            debug_range(wire_codes[r], n, true);
+            debug_range(wire_scales[r], blocks_of(n, block) * sizeof(float), true);
+        }
+    }
+    if (block && shard_codes != nullptr) {
+        debug_range(shard_codes, n, true);
+        debug_range(shard_scales, blocks_of(n, block) * sizeof(float), true);
+    }
+}
+
 int dda_common(const void *const *in, void *const *out, int nranks, size_t n,
                int dtype, int block, uint8_t *const *wire_codes,
                float *const *wire_scales, uint8_t *shard_codes, float *shard_scales,
@@ -177,6 +148,8 @@ int dda_common(const void *const *in, void *const *out, int nranks, size_t n,
     }
     p.shard_codes = (lp && tree) ? shard_codes : nullptr;
     p.shard_scales = (lp && tree) ? shard_scales : nullptr;
+    debug_dda_ranges(in, out, nranks, n, dtype, block, wire_codes, wire_scales, p.shard_codes,
+                     p.shard_scales);
     const int mode = !lp ? kExact : (tree ? kTree : kFlat);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return finish(dtype == LPCOLL_F32 ? launch_dda_f32(p, nranks, n, mode, s)
@@ -239,19 +212,64 @@ int check_common(int dtype, int nranks, int block)
     return LPCOLL_OK;
 }
 
+#ifdef LPCOLL_DEBUG_BOUNDS
+// The bounds-check record that kernels write (managed memory, one per
+// process) and the buffer list of the calling thread's current call.
+struct DebugRecord {
+    unsigned int flag;
+    unsigned int pad;
+    unsigned long long first_bad;
+};
+std::mutex g_record_mutex;
+DebugRecord *g_record = nullptr;
+thread_local DebugRanges g_pending = {};
+// lpcoll_debug_bounds_shrink: bytes taken off every buffer of the next call
+std::atomic<size_t> g_shrink_next{0};
+thread_local size_t g_shrink = 0;
+
+DebugRecord *debug_record()
+{
+    std::lock_guard<std::mutex> lock(g_record_mutex);
+    if (g_record == nullptr) {
+        void *p = nullptr;
+        if (cudaMallocManaged(&p, sizeof(DebugRecord)) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_record = static_cast<DebugRecord *>(p);
+        g_record->flag = 0;
+        g_record->first_bad = 0;
+    }
+    return g_record;
+}
+#endif
+
 }  // namespace
 
-void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
-
-int resident_ctas(const void *kernel, size_t smem) { return occupancy(kernel, smem).second; }
-
-int wave_ctas(const void *kernel, size_t units, int cap, size_t smem)
+#ifdef LPCOLL_DEBUG_BOUNDS
+void debug_begin()
 {
-    const size_t need = (units + kWarpsPerCta - 1) / kWarpsPerCta;
-    const size_t wave = static_cast<size_t>(full_wave(kernel, cap, smem));
-    const size_t g = need < wave ? need : wave;
-    return static_cast<int>(g < 1 ? 1 : g);
+    DebugRecord *rec = debug_record();
+    g_shrink = g_shrink_next.exchange(0);
+    g_pending.count = 0;
+    g_pending.flag = rec != nullptr ? &rec->flag : nullptr;
+    g_pending.first_bad = rec != nullptr ? &rec->first_bad : nullptr;
 }
+
+void debug_range(const void *p, size_t bytes, bool writable)
+{
+    if (p == nullptr || g_pending.count >= kDebugMaxRanges)
+        return;
+    const int i = g_pending.count++;
+    g_pending.lo[i] = static_cast<const char *>(p);
+    g_pending.hi[i] = static_cast<const char *>(p) + (bytes > g_shrink ? bytes - g_shrink : 0);
+    g_pending.writable[i] = writable ? 1 : 0;
+}
+
+const DebugRanges &debug_pending() { return g_pending; }
+#endif
+
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
 
 }  // namespace lpc
 
@@ -271,6 +289,10 @@ int lp_quantize(const void *in, lpcoll_dtype dtype, size_t n, int block,
     int st = first_error({check_ptr(in), check_ptr(codes), check_ptr(scales)});
     if (st != LPCOLL_OK)
         return st;
+    debug_begin();
+    debug_range(in, n * elem_bytes(dtype), false);
+    debug_range(codes, n, true);
+    debug_range(scales, blocks_of(n, block) * sizeof(float), true);
     return finish(launch_quantize(in, dtype, n, codes, scales,
                                   static_cast<cudaStream_t>(stream)));
 }
@@ -287,6 +309,10 @@ int lp_dequantize(const uint8_t *codes, const float *scales, size_t n, int block
     int st = first_error({check_ptr(codes), check_ptr(scales), check_ptr(out)});
     if (st != LPCOLL_OK)
         return st;
+    debug_begin();
+    debug_range(codes, n, false);
+    debug_range(scales, blocks_of(n, block) * sizeof(float), false);
+    debug_range(out, n * elem_bytes(dtype), true);
     return finish(launch_dequantize(codes, scales, n, out, dtype,
                                     static_cast<cudaStream_t>(stream)));
 }
@@ -305,10 +331,14 @@ int lp_reduce(const uint8_t *const *codes, const float *const *scales, int nrank
     if (st != LPCOLL_OK)
         return st;
     ReduceParams p = {};
+    debug_begin();
     for (int r = 0; r < nranks; ++r) {
         p.codes[r] = codes[r];
         p.scales[r] = scales[r];
+        debug_range(codes[r], n, false);
+        debug_range(scales[r], blocks_of(n, block) * sizeof(float), false);
     }
+    debug_range(out, n * elem_bytes(dtype), true);
     return finish(launch_reduce(p, nranks, n, out, dtype,
                                 static_cast<cudaStream_t>(stream)));
 }
@@ -346,6 +376,17 @@ int reduce_scatter_sim(const void *const *in, void *const *out, int nranks, size
     if (st != LPCOLL_OK)
         return st;
     p.shard_len = per;
+    debug_begin();
+    for (int r = 0; r < nranks; ++r) {
+        const size_t lo = static_cast<size_t>(r) * per;
+        debug_range(in[r], n * elem_bytes(dtype), false);
+        if (lo < n)
+            debug_range(out[r], (n - lo < per ? n - lo : per) * elem_bytes(dtype), true);
+        if (block) {
+            debug_range(wire_codes[r], n, true);
+            debug_range(wire_scales[r], blocks_of(n, block) * sizeof(float), true);
+        }
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return finish(dtype == LPCOLL_F32 ? launch_scatter_f32(p, nranks, n, block != 0, s)
                                       : launch_scatter_bf16(p, nranks, n, block != 0, s));
@@ -363,6 +404,15 @@ int all_gather_sim(const void *const *in, void *const *out, int nranks, size_t m
                          [](int) { return false; }, p);
     if (st != LPCOLL_OK)
         return st;
+    debug_begin();
+    for (int r = 0; r < nranks; ++r) {
+        debug_range(in[r], m * elem_bytes(dtype), false);
+        debug_range(out[r], static_cast<size_t>(nranks) * m * elem_bytes(dtype), true);
+        if (block) {
+            debug_range(wire_codes[r], m, true);
+            debug_range(wire_scales[r], blocks_of(m, block) * sizeof(float), true);
+        }
+    }
     return finish(launch_all_gather(p, nranks, m, dtype, block != 0,
                                     static_cast<cudaStream_t>(stream)));
 }
@@ -379,6 +429,17 @@ int all_to_all_sim(const void *const *in, void *const *out, int nranks, size_t c
                          [](int) { return false; }, p);
     if (st != LPCOLL_OK)
         return st;
+    debug_begin();
+    for (int r = 0; r < nranks; ++r) {
+        const size_t all = static_cast<size_t>(nranks) * c;
+        debug_range(in[r], all * elem_bytes(dtype), false);
+        debug_range(out[r], all * elem_bytes(dtype), true);
+        if (block) {
+            debug_range(wire_codes[r], all, true);
+            debug_range(wire_scales[r],
+                        static_cast<size_t>(nranks) * blocks_of(c, block) * sizeof(float), true);
+        }
+    }
     return finish(launch_all_to_all(p, nranks, c, dtype, block != 0,
                                     static_cast<cudaStream_t>(stream)));
 }
@@ -392,6 +453,10 @@ int lp_quantize_fmt(const void *in, lpcoll_dtype dtype, size_t n, int block,
     st = first_error({check_ptr(in), check_ptr(codes), check_ptr(scales)});
     if (st != LPCOLL_OK)
         return st;
+    debug_begin();
+    debug_range(in, n * elem_bytes(dtype), false);
+    debug_range(codes, n, true);
+    debug_range(scales, blocks_of(n, block) * sizeof(float), true);
     return finish(launch_quantize_fmt(in, dtype, n, block, fmt, codes, scales,
                                       static_cast<cudaStream_t>(stream)));
 }
@@ -405,6 +470,10 @@ int lp_dequantize_fmt(const uint8_t *codes, const float *scales, size_t n, int b
     st = first_error({check_ptr(codes), check_ptr(scales), check_ptr(out)});
     if (st != LPCOLL_OK)
         return st;
+    debug_begin();
+    debug_range(codes, n, false);
+    debug_range(scales, blocks_of(n, block) * sizeof(float), false);
+    debug_range(out, n * elem_bytes(dtype), true);
     return finish(launch_dequantize_fmt(codes, scales, n, block, fmt, out, dtype,
                                         static_cast<cudaStream_t>(stream)));
 }
@@ -423,10 +492,14 @@ int lp_reduce_fmt(const uint8_t *const *codes, const float *const *scales, int n
     if (st != LPCOLL_OK)
         return st;
     ReduceParams p = {};
+    debug_begin();
     for (int r = 0; r < nranks; ++r) {
         p.codes[r] = codes[r];
         p.scales[r] = scales[r];
+        debug_range(codes[r], n, false);
+        debug_range(scales[r], blocks_of(n, block) * sizeof(float), false);
     }
+    debug_range(out, n * elem_bytes(dtype), true);
     return finish(launch_reduce_fmt(p, nranks, n, block, fmt, out, dtype,
                                     static_cast<cudaStream_t>(stream)));
 }
@@ -445,6 +518,39 @@ const char *lpcoll_status_string(int status)
 }
 
 int lpcoll_last_cuda_error(void) { return g_last_cuda_error; }
+
+int lpcoll_debug_bounds_errors(unsigned long long *first_bad)
+{
+    if (first_bad != nullptr)
+        *first_bad = 0;
+#ifdef LPCOLL_DEBUG_BOUNDS
+    const cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return -2;
+    }
+    DebugRecord *rec = debug_record();
+    if (rec == nullptr)
+        return -2;
+    const int bad = rec->flag != 0 ? 1 : 0;
+    if (first_bad != nullptr)
+        *first_bad = rec->first_bad;
+    rec->flag = 0;
+    rec->first_bad = 0;
+    return bad;
+#else
+    return -1;
+#endif
+}
+
+void lpcoll_debug_bounds_shrink(size_t bytes)
+{
+#ifdef LPCOLL_DEBUG_BOUNDS
+    g_shrink_next.store(bytes);
+#else
+    (void)bytes;
+#endif
+}
 
 int lpcoll_version(void) { return 100; }
 

@@ -26,9 +26,6 @@ namespace lpc {
 // iteration are issued before any of its units is processed (+52% over one
 // unit per iteration on GB300; 8 units: slower).
 constexpr int kDequantizeUnits = 4;
-// The quantize kernel reads four times what it writes and takes all the
-// resident CTAs it can get (up to 8 per SM: +10% over 4).
-constexpr int kQuantizeCtasPerSm = 8;
 // Warp-units [u0, u0 + K) of one message of n elements; e0 / cnt per lane.
 template <int DT, int K>
 __device__ __forceinline__ void unit_lanes(size_t n, size_t u0, int lane, size_t (&e0)[K],
@@ -69,7 +66,7 @@ quantize_kernel(const void *in, uint8_t *codes, float *scales, size_t n, size_t 
         if (e0 < n) {
             wide_store_codes(codes, n, e0, w);
             if (lane % G == 0)
-                __stcs(scales + e0 / (kWideElems * G), s);
+                store_scale(scales + e0 / (kWideElems * G), s);
         }
     }
 }
@@ -95,7 +92,7 @@ dequantize_kernel(const uint8_t *codes, const float *scales, void *out, size_t n
         for (int k = 0; k < K; ++k) {
             if (cnt[k] > 0) {
                 c[k] = load_codes<DT>(codes, e0[k], cnt[k]);
-                s[k] = scales[e0[k] / kBlock];
+                s[k] = load_scale(scales + e0[k] / kBlock);
             }
         }
 #pragma unroll
@@ -129,7 +126,7 @@ reduce_kernel(const __grid_constant__ ReduceParams p, void *out, size_t n, size_
 #pragma unroll
             for (int r = 0; r < N; ++r) {
                 c[r] = wide_load_codes(p.codes[r], n, e0);
-                s[r] = p.scales[r][e0 / kBlock];
+                s[r] = load_scale(p.scales[r] + e0 / kBlock);
             }
 #pragma unroll
             for (int r = 0; r < N; ++r) {
@@ -165,10 +162,8 @@ cudaError_t launch_quantize_t(const void *in, uint8_t *codes, float *scales, siz
                               cudaStream_t stream)
 {
     const size_t items = wide_items(n);
-    const int grid = wave_ctas(reinterpret_cast<const void *>(&quantize_kernel<DT, FMT, G>),
-                               items, kQuantizeCtasPerSm);
-    return launch_kernel(quantize_kernel<DT, FMT, G>, grid, stream, in, codes, scales, n,
-                         items);
+    return launch_kernel(quantize_kernel<DT, FMT, G>, item_ctas(items), stream, in, codes,
+                         scales, n, items);
 }
 
 // Block size (32, 64, 128 or 256 elements) -> lanes per block.
@@ -190,9 +185,8 @@ cudaError_t launch_dequantize_t(const uint8_t *codes, const float *scales, void 
                                 size_t n, cudaStream_t stream)
 {
     const size_t items = items_of<DT, kDequantizeUnits>(n);
-    const int grid =
-        wave_ctas(reinterpret_cast<const void *>(&dequantize_kernel<DT>), items);
-    return launch_kernel(dequantize_kernel<DT>, grid, stream, codes, scales, out, n, items);
+    return launch_kernel(dequantize_kernel<DT>, item_ctas(items), stream, codes, scales, out,
+                         n, items);
 }
 
 template <int N, int DT>
@@ -200,9 +194,7 @@ cudaError_t launch_reduce_n(const ReduceParams &p, void *out, size_t n,
                             cudaStream_t stream)
 {
     const size_t items = wide_items(n);
-    const int grid =
-        wave_ctas(reinterpret_cast<const void *>(&reduce_kernel<N, DT>), items);
-    return launch_kernel(reduce_kernel<N, DT>, grid, stream, p, out, n, items);
+    return launch_kernel(reduce_kernel<N, DT>, item_ctas(items), stream, p, out, n, items);
 }
 
 template <int DT>

@@ -17,18 +17,17 @@
 // Every element is read before any output of its unit is written, so an
 // output may alias its input.
 //
-// The warps stride over units (grid-stride loop); the grid is at most 2 CTAs
-// per SM for large allreduces and 4 otherwise (kCtasPerSm / kCtasPerSmBusy),
-// all resident at once, so the units of every rank stream through HBM in
-// order.
+// The grid has one warp per unit (or per group of units, see
+// units_per_iter): item_ctas in lpcoll_device.cuh. The warps still stride
+// over units, so any grid is correct, and no CTA waits on another.
 //
 // Tile path (TILES; see tile_path_built for where it is used): a CTA
-// instead takes a tile of kTileUnits consecutive units per iteration (one
-// per warp), builds the tile's outputs, codes and scales in a double-buffered
-// shared-memory area, and one thread writes each of them with a single bulk
-// copy (cp.async.bulk.global.shared::cta). The loads and the arithmetic are
-// the same as on the direct path; only where the results go differs (the
-// sink), so both paths give bit-identical results.
+// instead takes a tile of kTileUnits consecutive units (one per warp; one
+// tile per CTA with the item_ctas grid), builds the tile's outputs, codes
+// and scales in a shared-memory area, and one thread writes each of them
+// with a single bulk copy (cp.async.bulk.global.shared::cta). The loads and
+// the arithmetic are the same as on the direct path; only where the results
+// go differs (the sink), so both paths give bit-identical results.
 #pragma once
 
 #include "lpcoll_device.cuh"
@@ -57,10 +56,13 @@ __device__ __forceinline__ void scatter_store(const DdaParams &p, size_t e0, int
         const size_t e = e0 + j;
         const size_t o = e / L;
         if (DT == LPCOLL_F32) {
-            static_cast<uint32_t *>(p.out[o])[e - o * L] = w[j];
+            uint32_t *q = static_cast<uint32_t *>(p.out[o]) + (e - o * L);
+            if (LPC_WRITE_OK(q, 4))
+                *q = w[j];
         } else {
-            static_cast<uint16_t *>(p.out[o])[e - o * L] =
-                static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+            uint16_t *q = static_cast<uint16_t *>(p.out[o]) + (e - o * L);
+            if (LPC_WRITE_OK(q, 2))
+                *q = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
         }
     }
 }
@@ -119,7 +121,7 @@ struct GlobalSink {
     }
     __device__ __forceinline__ void scale(int r, float s) const
     {
-        __stcs(p.scales[r] + e0 / kBlock, s);
+        store_scale(p.scales[r] + e0 / kBlock, s);
     }
     __device__ __forceinline__ void shard_codes(Codes<DT> c) const
     {
@@ -127,7 +129,7 @@ struct GlobalSink {
     }
     __device__ __forceinline__ void shard_scale(float s) const
     {
-        __stcs(p.shard_scales + e0 / kBlock, s);
+        store_scale(p.shard_scales + e0 / kBlock, s);
     }
     __device__ __forceinline__ void out(uint4 o) const
     {
@@ -312,6 +314,8 @@ __device__ __forceinline__ void dda_units(const DdaParams &p, size_t unit0, int 
 // completion is tracked with commit / wait groups.
 __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes)
 {
+    if (!LPC_WRITE_OK(gdst, bytes))
+        return;
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
                  "r"(static_cast<uint32_t>(__cvta_generic_to_shared(ssrc))), "r"(bytes)
                  : "memory");
@@ -415,27 +419,17 @@ inline void unit_counts(size_t n, size_t &full, size_t &total)
     total = (n + per - 1) / per;
 }
 
-// CTAs for a launch covering `units` warp-units: enough for every unit, at
-// most min(resident CTAs per SM, cap) x SMs (occupancy with `smem` bytes of
-// dynamic shared memory per CTA).
-int wave_ctas(const void *kernel, size_t units, int cap = kCtasPerSmBusy, size_t smem = 0);
-
-// Resident CTAs per SM of a kernel with `smem` bytes of dynamic shared
-// memory (cached per kernel, device and size).
-int resident_ctas(const void *kernel, size_t smem);
-
 // Tile path policy, from measurements on GB300 (CUDA events, L2 flushed,
-// LP, tile path against the direct path):
-//   FP32, 8 ranks: 256 MiB of input 97.8 -> 100.4 us (flat), 512 MiB equal,
-//     1 GiB 381.5 -> 372.8 us, 2 GiB 761.6 -> 733.4 us (flat) and
-//     783.9 -> 760.9 us (tree), 4 GiB 1513 -> 1460 us;
-//   FP32, 12 ranks: 3-7% slower at every size from 256 MiB to 4 GiB;
-//   FP32, 16 ranks: 7-11% slower (98 registers leave 2 CTAs per SM);
-//   FP32, 4 ranks (4 loads per lane instead of the direct path's 8): 7% slower;
-//   BF16, 8 ranks, 128 and 512 MiB: equal; the exact allreduce: equal.
-// So it is taken for FP32 LP allreduces of 8 ranks and 1 GiB of input or
-// more, when kTileCtasPerSm CTAs fit on an SM; everything else stays direct.
-constexpr int kTileCtasPerSm = 3;
+// LP, tile path against the direct path, both with the item_ctas grid):
+//   FP32, 8 ranks: up to 512 MiB of input equal or slower (128 MiB flat
+//     45.7 -> 47.7 us), 1 GiB equal (flat) / 1% faster (tree), 2 GiB
+//     694.9 -> 688.8 us (flat) and 707.2 -> 697.0 us (tree), 4 GiB 1.1-1.2%
+//     faster;
+//   BF16, 8 ranks, 64 MiB to 1 GiB: equal or slower.
+// With grids of 2-3 resident CTAs per SM (measured before item_ctas) it was
+// also slower with 4, 12 and 16 ranks (4-11%) and equal for the exact
+// allreduce. So it is taken for FP32 LP allreduces of 8 ranks and 1 GiB of
+// input or more; everything else stays direct.
 constexpr size_t kTileMinBytes = size_t(1) << 30;
 template <int N, int DT, int MODE>
 constexpr bool tile_path_built()
@@ -453,20 +447,17 @@ cudaError_t launch_dda_n(const DdaParams &p, size_t n, cudaStream_t stream)
         const size_t tiles = full / kTileUnits;
         constexpr size_t smem = 2 * static_cast<size_t>(TileLayout<N, DT>::kBytes);
         static_assert(smem <= 48 * 1024, "tile buffers must fit the default dynamic smem");
-        auto *kt = &dda_kernel<N, DT, MODE, true>;
-        const void *ktv = reinterpret_cast<const void *>(kt);
-        if (bytes >= kTileMinBytes && tiles > 0 && resident_ctas(ktv, smem) >= kTileCtasPerSm) {
-            const int grid = wave_ctas(ktv, tiles * kWarpsPerCta, kTileCtasPerSm, smem);
-            return launch_kernel_smem(kt, grid, smem, stream, p, n, full, total);
+        if (bytes >= kTileMinBytes && tiles > 0) {
+            // one tile per CTA, plus the warps for the units after the last tile
+            const size_t rest = total - tiles * kTileUnits;
+            const int grid = item_ctas(tiles * kWarpsPerCta > rest ? tiles * kWarpsPerCta : rest);
+            return launch_kernel_smem(dda_kernel<N, DT, MODE, true>, grid, smem, stream, p, n,
+                                      full, total);
         }
     }
-    const void *k = reinterpret_cast<const void *>(&dda_kernel<N, DT, MODE, false>);
     const size_t K = units_per_iter<N>();
-    const bool scatter = (MODE == kScatterExact || MODE == kScatterLp);
-    const size_t in_bytes = n * static_cast<size_t>(N) * (16 / Fmt<DT>::kVec);
-    const int cap = (scatter || in_bytes < kSmallLaunchBytes) ? kCtasPerSmBusy : kCtasPerSm;
-    const int grid = wave_ctas(k, (total + K - 1) / K, cap);
-    return launch_kernel(dda_kernel<N, DT, MODE, false>, grid, stream, p, n, full, total);
+    return launch_kernel(dda_kernel<N, DT, MODE, false>, item_ctas((total + K - 1) / K), stream,
+                         p, n, full, total);
 }
 
 template <int DT, int MODE>

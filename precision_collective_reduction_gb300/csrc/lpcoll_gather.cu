@@ -58,7 +58,7 @@ __device__ __forceinline__ void encode_item(const DdaParams &p, int r, size_t co
                 store_codes(p.codes[r], code_base + e0[k], access_count<DT>(cnt[k], aligned),
                             c);
                 if ((lane % Fmt<DT>::kGroup) == 0)
-                    __stcs(p.scales[r] + scale_base + e0[k] / kBlock, s);
+                    store_scale(p.scales[r] + scale_base + e0[k] / kBlock, s);
             }
             dequantize_lane<DT>(c, s, x[k]);
         }
@@ -123,9 +123,9 @@ gather_kernel(const __grid_constant__ DdaParams p, int nranks, size_t m, size_t 
 // units after a sender's last full tile are stored directly. Measured on
 // GB300 against the item kernel above (8 ranks, CUDA events, L2 flushed):
 // 1 Mi BF16 contributions 28.7 -> 28.7 us, 4 Mi BF16 108.5 -> 102.4 us,
-// 8 Mi FP32 420.1 -> 386.7 us (6427 GB/s); 3 CTAs per SM (2 or 4: 3-6%
-// slower), one unit per warp (2 or 4 units: slower above 1 Mi).
-constexpr int kAgTileCtasPerSm = 3;
+// 8 Mi FP32 420.1 -> 386.7 us (6427 GB/s), both with grids of 3 resident
+// CTAs per SM (2 or 4: 3-6% slower); one unit per warp (2 or 4 units: slower
+// above 1 Mi). The grid has one CTA per tile (item_ctas).
 template <int DT>
 struct AgTile {
     static constexpr int kUnits = kWarpsPerCta;
@@ -204,7 +204,7 @@ gather_tile_kernel(const __grid_constant__ DdaParams p, int nranks, size_t m,
         if (cnt > 0) {
             store_codes(p.codes[r], e0, cnt, c);
             if ((lane % Fmt<DT>::kGroup) == 0)
-                __stcs(p.scales[r] + e0 / kBlock, s);
+                store_scale(p.scales[r] + e0 / kBlock, s);
             const uint4 o = narrow<DT>(x);
             for (int d = 0; d < nranks; ++d)
                 store_vec<DT>(p.out[d], static_cast<size_t>(r) * m + e0, cnt, o);
@@ -257,9 +257,11 @@ alltoall_kernel(const __grid_constant__ DdaParams p, int nranks, size_t c, size_
 }
 
 // Low-precision AlltoAll, per element format: wide items per warp step (all
-// their loads issued first) and resident CTAs per SM. Measured on GB300 with
-// 8 ranks: FP32 1 item at 3 CTAs per SM (2 CTAs: -17%; 2 items: -1%), BF16
-// 2 items at 4 CTAs per SM (1 item: -20%; 4 items: -3%; 3 CTAs: -4%).
+// their loads issued first) and the resident CTAs per SM the registers are
+// budgeted for (__launch_bounds__). Measured on GB300 with 8 ranks, on grids
+// of that many resident CTAs per SM: FP32 1 item at 3 CTAs per SM (2 CTAs:
+// -17%; 2 items: -1%), BF16 2 items at 4 CTAs per SM (1 item: -20%; 4 items:
+// -3%; 3 CTAs: -4%). The grid has one warp per step (item_ctas).
 template <int DT> struct A2aLp;
 template <> struct A2aLp<LPCOLL_F32> {
     static constexpr int kItems = 1;
@@ -308,7 +310,7 @@ __device__ __forceinline__ void alltoall_lp_step(const DdaParams &p, size_t c, s
         if (e0[k] < c) {
             wide_store_codes(p.codes[r] + src, c, e0[k], w);
             if (lane % kWideGroup == 0)
-                __stcs(p.scales[r] + static_cast<size_t>(j) * nbc + e0[k] / kBlock, s);
+                store_scale(p.scales[r] + static_cast<size_t>(j) * nbc + e0[k] / kBlock, s);
         }
         wide_dequant(make_uint4(w[0], w[1], w[2], w[3]), s, x);
         wide_store_results<DT, ALIGNED>(out, c, (g * K + k) * kWideItem, x, stage, lane);
@@ -360,15 +362,13 @@ cudaError_t launch_gather_t(const DdaParams &p, int nranks, size_t m, cudaStream
         const size_t tail_units = static_cast<size_t>(nranks) * (units - tps * L::kUnits);
         const size_t need = std::max(static_cast<size_t>(nranks) * tps,
                                      (tail_units + kWarpsPerCta - 1) / kWarpsPerCta);
-        auto *k = &gather_tile_kernel<DT>;
-        const int grid = wave_ctas(reinterpret_cast<const void *>(k), need * kWarpsPerCta,
-                                   kAgTileCtasPerSm, smem);
-        return launch_kernel_smem(k, grid, smem, st, p, nranks, m, tps, units);
+        return launch_kernel_smem(gather_tile_kernel<DT>, item_ctas(need * kWarpsPerCta), smem,
+                                  st, p, nranks, m, tps, units);
     }
     const size_t groups = item_groups<DT>(m);
-    const void *k = reinterpret_cast<const void *>(&gather_kernel<DT, LP, ALIGNED>);
-    const int grid = wave_ctas(k, groups * static_cast<size_t>(nranks));
-    return launch_kernel(gather_kernel<DT, LP, ALIGNED>, grid, st, p, nranks, m, groups);
+    return launch_kernel(gather_kernel<DT, LP, ALIGNED>,
+                         item_ctas(groups * static_cast<size_t>(nranks)), st, p, nranks, m,
+                         groups);
 }
 
 template <int DT, bool LP, bool ALIGNED>
@@ -379,15 +379,12 @@ cudaError_t launch_alltoall_t(const DdaParams &p, int nranks, size_t c, cudaStre
         const size_t per = static_cast<size_t>(kWideItem) * A2aLp<DT>::kItems;
         const size_t groups = (c + per - 1) / per;
         const size_t nbc = (c + kBlock - 1) / kBlock;
-        const void *k = reinterpret_cast<const void *>(&alltoall_lp_kernel<DT, ALIGNED>);
-        const int grid = wave_ctas(k, groups * pairs, A2aLp<DT>::kCtas);
-        return launch_kernel(alltoall_lp_kernel<DT, ALIGNED>, grid, st, p, nranks, c, nbc,
-                             groups);
+        return launch_kernel(alltoall_lp_kernel<DT, ALIGNED>, item_ctas(groups * pairs), st, p,
+                             nranks, c, nbc, groups);
     } else {
         const size_t groups = item_groups<DT>(c);
-        const void *k = reinterpret_cast<const void *>(&alltoall_kernel<DT, ALIGNED>);
-        const int grid = wave_ctas(k, groups * pairs);
-        return launch_kernel(alltoall_kernel<DT, ALIGNED>, grid, st, p, nranks, c, groups);
+        return launch_kernel(alltoall_kernel<DT, ALIGNED>, item_ctas(groups * pairs), st, p,
+                             nranks, c, groups);
     }
 }
 

@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <initializer_list>
 #include <vector>
 
@@ -30,6 +31,29 @@ namespace {
 
 constexpr size_t kAlign = 256;  // every sub-buffer of a slot starts 256-aligned
 constexpr int kMaxSlots = 8;
+
+// Test hook (lpcoll_debug_fail_host_enqueue): the index of the enqueue step
+// of the next lpcoll_host_allreduce call that reports an error instead of
+// calling CUDA, or -1.
+std::atomic<long> g_fail_step{-1};
+
+// Error code that an injected failure reports.
+constexpr cudaError_t kInjectedError = cudaErrorInvalidValue;
+
+// The enqueue steps of one call (copies, event records and waits, launches),
+// counted so that a test can make the k-th one fail on the host.
+struct Steps {
+    long next = 0;
+    long fail_at;
+    Steps() : fail_at(g_fail_step.exchange(-1)) {}
+    template <class F>
+    void run(cudaError_t &e, F &&f)
+    {
+        if (e != cudaSuccess)
+            return;
+        e = (next++ == fail_at) ? kInjectedError : f();
+    }
+};
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -111,6 +135,11 @@ cudaError_t launch_chunk(const Slot &s, bool tree, int nranks, size_t m, int dty
 
 using namespace lpc;
 
+extern "C" void lpcoll_debug_fail_host_enqueue(long step)
+{
+    g_fail_step.store(step < 0 ? -1 : step);
+}
+
 extern "C" size_t lpcoll_host_workspace_bytes(int nranks, size_t chunk, lpcoll_dtype dtype,
                                               int block, int flat, int tree, int slots)
 {
@@ -160,6 +189,8 @@ extern "C" int lpcoll_host_allreduce(const void *const *host_in, void *const *ho
 
     std::vector<Slot> slot(S);
     cudaError_t e = cudaSuccess;
+    debug_begin();  // the kernels touch nothing but the workspace
+    debug_range(workspace, workspace_bytes, true);
     for (int i = 0; i < S; ++i) {
         Slot &s = slot[i];
         carve(s, static_cast<char *>(workspace) + L.bytes * i, L, nranks, block);
@@ -173,43 +204,53 @@ extern "C" int lpcoll_host_allreduce(const void *const *host_in, void *const *ho
             e = cudaEventCreateWithFlags(&s.out_done, cudaEventDisableTiming);
     }
 
+    Steps step;
     for (size_t k = 0; k < nchunks && e == cudaSuccess; ++k) {
         Slot &s = slot[k % S];
         const size_t lo = k * chunk;
         const size_t m = (n - lo < chunk) ? n - lo : chunk;
         if (s.used)
-            e = cudaStreamWaitEvent(s_in, s.out_done, 0);
-        for (int r = 0; r < nranks && e == cudaSuccess; ++r)
-            e = cudaMemcpyAsync(s.in[r], static_cast<const char *>(host_in[r]) + lo * es,
-                                m * es, cudaMemcpyHostToDevice, s_in);
-        if (e == cudaSuccess)
-            e = cudaEventRecord(s.in_done, s_in);
-        if (e == cudaSuccess)
-            e = cudaStreamWaitEvent(s_cmp, s.in_done, 0);
-        if (e == cudaSuccess && flat)
-            e = launch_chunk(s, false, nranks, m, dtype, block, s_cmp);
-        if (e == cudaSuccess && tree)
-            e = launch_chunk(s, true, nranks, m, dtype, block, s_cmp);
-        if (e == cudaSuccess)
-            e = cudaEventRecord(s.computed, s_cmp);
-        if (e == cudaSuccess)
-            e = cudaStreamWaitEvent(s_out, s.computed, 0);
-        for (int r = 0; r < nranks && e == cudaSuccess; ++r) {
+            step.run(e, [&] { return cudaStreamWaitEvent(s_in, s.out_done, 0); });
+        for (int r = 0; r < nranks; ++r)
+            step.run(e, [&] {
+                return cudaMemcpyAsync(s.in[r], static_cast<const char *>(host_in[r]) + lo * es,
+                                       m * es, cudaMemcpyHostToDevice, s_in);
+            });
+        step.run(e, [&] { return cudaEventRecord(s.in_done, s_in); });
+        step.run(e, [&] { return cudaStreamWaitEvent(s_cmp, s.in_done, 0); });
+        if (flat)
+            step.run(e, [&] { return launch_chunk(s, false, nranks, m, dtype, block, s_cmp); });
+        if (tree)
+            step.run(e, [&] { return launch_chunk(s, true, nranks, m, dtype, block, s_cmp); });
+        step.run(e, [&] { return cudaEventRecord(s.computed, s_cmp); });
+        step.run(e, [&] { return cudaStreamWaitEvent(s_out, s.computed, 0); });
+        for (int r = 0; r < nranks; ++r) {
             if (flat)
-                e = cudaMemcpyAsync(static_cast<char *>(host_out_flat[r]) + lo * es,
-                                    s.out_flat[r], m * es, cudaMemcpyDeviceToHost, s_out);
-            if (e == cudaSuccess && tree)
-                e = cudaMemcpyAsync(static_cast<char *>(host_out_tree[r]) + lo * es,
-                                    s.out_tree[r], m * es, cudaMemcpyDeviceToHost, s_out);
+                step.run(e, [&] {
+                    return cudaMemcpyAsync(static_cast<char *>(host_out_flat[r]) + lo * es,
+                                           s.out_flat[r], m * es, cudaMemcpyDeviceToHost, s_out);
+                });
+            if (tree)
+                step.run(e, [&] {
+                    return cudaMemcpyAsync(static_cast<char *>(host_out_tree[r]) + lo * es,
+                                           s.out_tree[r], m * es, cudaMemcpyDeviceToHost, s_out);
+                });
         }
-        if (e == cudaSuccess)
-            e = cudaEventRecord(s.out_done, s_out);
+        step.run(e, [&] { return cudaEventRecord(s.out_done, s_out); });
         s.used = true;
     }
-    // the results are in host memory only once the copy-out stream has drained
+    // On success the results are in host memory once the copy-out stream has
+    // drained. After an error, part of the pipeline may still be queued on
+    // the other two streams (copies reading the caller's host inputs, kernels
+    // writing the workspace): wait for all three, so that nothing this call
+    // queued still touches the caller's buffers when it returns.
     const cudaError_t sync = cudaStreamSynchronize(s_out);
     if (e == cudaSuccess)
         e = sync;
+    if (e != cudaSuccess) {
+        cudaStreamSynchronize(s_in);
+        cudaStreamSynchronize(s_cmp);
+    }
     for (Slot &s : slot)
         for (cudaEvent_t ev : {s.in_done, s.computed, s.out_done})
             if (ev != nullptr)

@@ -15,7 +15,10 @@
 // the process exits. Host code cannot use the array's name as a device
 // address (on the host it names a host-side shadow), so the address is looked
 // up once per device with cudaGetSymbolAddress, with that device current, on
-// the first call made while it is current.
+// the first call made while it is current. The cached address belongs to
+// the device's current context: after cudaDeviceReset (or any other
+// teardown of that context) it is stale, so the library must not be used
+// across a device reset.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -90,21 +93,34 @@ extern "C" int dda_flat_sim_noalloc(const void *const *in, void *const *out,
 
     unsigned char *base = nullptr;
     cudaError_t e = scratch_address(&base);
-    if (e != cudaSuccess)
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        lpc::record_cuda_error(e);
         return LPCOLL_ERR_CUDA;
+    }
     const size_t scale_stride = round_up((n + LPCOLL_BLOCK - 1) / LPCOLL_BLOCK,
                                          kRankAlign / sizeof(float));
     float *scales = reinterpret_cast<float *>(base + kCodeBytes);
 
     lpc::DdaParams p = {};
+    const size_t es = dtype == LPCOLL_F32 ? 4 : 2;
+    lpc::debug_begin();
+    lpc::debug_range(base, kScratchBytes, true);
     for (int r = 0; r < nranks; ++r) {
         p.in[r] = in[r];
         p.out[r] = out[r];
         p.codes[r] = base + static_cast<size_t>(r) * code_stride;
         p.scales[r] = scales + static_cast<size_t>(r) * scale_stride;
+        lpc::debug_range(in[r], n * es, false);
+        lpc::debug_range(out[r], n * es, true);
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     e = dtype == LPCOLL_F32 ? lpc::launch_dda_f32(p, nranks, n, lpc::kFlat, s)
                             : lpc::launch_dda_bf16(p, nranks, n, lpc::kFlat, s);
-    return e == cudaSuccess ? LPCOLL_OK : LPCOLL_ERR_CUDA;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        lpc::record_cuda_error(e);
+        return LPCOLL_ERR_CUDA;
+    }
+    return LPCOLL_OK;
 }

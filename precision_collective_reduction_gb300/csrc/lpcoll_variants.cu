@@ -81,7 +81,7 @@ dequantize_fmt_kernel(const uint8_t *codes, const float *scales, void *out, size
             cnt[k] = lane_count<DT>(n, e0[k]);
             if (cnt[k] > 0) {
                 c[k] = load_codes<DT>(codes, e0[k], cnt[k]);
-                s[k] = scales[e0[k] / block];
+                s[k] = load_scale(scales + e0[k] / block);
             }
         }
 #pragma unroll
@@ -122,7 +122,7 @@ reduce_fmt_kernel(const __grid_constant__ ReduceParams p, int nranks, void *out,
                 for (int k = 0; k < kRankChunk; ++k) {
                     if (r0 + k < nranks) {
                         c[k] = wide_load_codes(p.codes[r0 + k], n, e0);
-                        s[k] = p.scales[r0 + k][b];
+                        s[k] = load_scale(p.scales[r0 + k] + b);
                     }
                 }
 #pragma unroll
@@ -148,9 +148,8 @@ cudaError_t dequantize_fmt_t(const uint8_t *codes, const float *scales, size_t n
     size_t full, units;
     unit_counts<DT>(n, full, units);
     const size_t groups = (units + kVariantUnits - 1) / kVariantUnits;
-    const void *k = reinterpret_cast<const void *>(&dequantize_fmt_kernel<DT, FMT>);
-    return launch_kernel(dequantize_fmt_kernel<DT, FMT>, wave_ctas(k, groups), st, codes,
-                         scales, out, n, block, groups);
+    return launch_kernel(dequantize_fmt_kernel<DT, FMT>, item_ctas(groups), st, codes, scales,
+                         out, n, block, groups);
 }
 
 template <int DT, int FMT>
@@ -161,8 +160,7 @@ cudaError_t reduce_fmt_t(const ReduceParams &p, int nranks, size_t n, int block,
     int shift = 0;
     while ((1 << shift) < block)
         ++shift;
-    const void *k = reinterpret_cast<const void *>(&reduce_fmt_kernel<DT, FMT>);
-    return launch_kernel(reduce_fmt_kernel<DT, FMT>, wave_ctas(k, items), st, p, nranks, out, n,
+    return launch_kernel(reduce_fmt_kernel<DT, FMT>, item_ctas(items), st, p, nranks, out, n,
                          shift, items);
 }
 

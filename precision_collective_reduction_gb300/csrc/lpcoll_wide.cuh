@@ -21,6 +21,8 @@ constexpr int kWideItem = 32 * kWideElems;
 // 16 codes of a wide lane starting at element e0 < n (missing ones read 0).
 __device__ __forceinline__ uint4 wide_load_codes(const uint8_t *codes, size_t n, size_t e0)
 {
+    if (!LPC_READ_OK(codes + e0, n - e0 < kWideElems ? n - e0 : kWideElems))
+        return make_uint4(0u, 0u, 0u, 0u);
     if (n - e0 >= kWideElems)
         return __ldcs(reinterpret_cast<const uint4 *>(codes + e0));
     const size_t c = n - e0;
@@ -37,6 +39,8 @@ __device__ __forceinline__ uint4 wide_load_codes(const uint8_t *codes, size_t n,
 __device__ __forceinline__ void wide_store_codes(uint8_t *codes, size_t n, size_t e0,
                                                  const uint32_t (&w)[4])
 {
+    if (!LPC_WRITE_OK(codes + e0, n - e0 < kWideElems ? n - e0 : kWideElems))
+        return;
     if (n - e0 >= kWideElems && (reinterpret_cast<uintptr_t>(codes + e0) & 15u) == 0) {
         __stcs(reinterpret_cast<uint4 *>(codes + e0), make_uint4(w[0], w[1], w[2], w[3]));
         return;

@@ -74,3 +74,34 @@ def test_direct_call_pageable_and_default_streams(oracle):
     want = oracle.flat(ins)[0]
     for r in range(N):
         assert same_bits(_np(hflat[r], W.BF16), want[r])
+
+
+@pytest.mark.parametrize("fail_step", [3, 10, 12, 25, 40, 61])
+def test_error_return_waits_for_every_stream(fail_step):
+    # A failure injected on the host at one enqueue step (no CUDA call
+    # fails) must not let the call return while work it queued before the
+    # failure still runs: on return, all three streams are idle, so the
+    # caller may free its host buffers and the workspace at once.
+    # 8 ranks x 16 Mi FP32 in chunks of 4 Mi: the copies of one chunk take
+    # milliseconds, far longer than the host needs to reach the return.
+    # Enqueue steps per chunk (flat only): 8 copies in, event record, wait,
+    # launch, record, wait, 8 copies out, record (+1 wait once a slot is
+    # reused), so the steps above land in the copy-in, launch, copy-out and
+    # second-chunk phases.
+    from precision_collective_reduction_gb300 import _binding as B
+    N, n = 8, 16 << 20
+    h = HostAllreduce(N, n, W.F32, 128, algos=("flat",), chunk=4 << 20, slots=2)
+    hin = [torch.full((n,), float(r), dtype=torch.float32).pin_memory() for r in range(N)]
+    hout = {"flat": [torch.empty(n, dtype=torch.float32).pin_memory() for _ in range(N)]}
+    torch.cuda.synchronize()
+    B.lib().lpcoll_debug_fail_host_enqueue(fail_step)
+    with pytest.raises(B.LpcollError) as err:
+        h.run(hin, hout)
+    assert err.value.status == 5  # LPCOLL_ERR_CUDA
+    idle = [s.query() for s in h.streams]
+    assert idle == [True, True, True], idle
+    assert B.lib().lpcoll_last_cuda_error() == 1  # cudaErrorInvalidValue, injected
+    # the hook fired once: the next call runs normally and is correct
+    h.run(hin, hout)
+    want = float(N * (N - 1) // 2)
+    assert all(bool((t == want).all()) for t in hout["flat"])
