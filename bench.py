@@ -479,8 +479,13 @@ def measure_collectives(torch, stream, iters=20):
     for kind, (fn, count) in calls.items():
         us = flushed_median_us(torch, stream, scratch, lambda: fn(stream), iters)
         nbytes = collective_bytes(kind, N, count, 2, 128)
+        gus = graph_us(torch, stream, lambda: fn(stream), 50)
         out[kind] = {"us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
-                     "bytes_alg": nbytes, "count_per_rank": count, "l2": "flushed"}
+                     "bytes_alg": nbytes, "count_per_rank": count, "l2": "flushed",
+                     "warm_us_per_call": round(back_to_back_us(torch, stream,
+                                                               lambda: fn(stream), 100), 3),
+                     "graph_us_per_call": round(gus, 3),
+                     "graph_GBps": round(nbytes / gus / 1e3, 1)}
     del ins, wc, ws, scratch, rs_out, full_out
     torch.cuda.empty_cache()
     return out

@@ -106,8 +106,20 @@ dequantize_kernel(const uint8_t *codes, const float *scales, void *out, size_t n
     }
 }
 
+// Resident CTAs per SM the reduce kernel's registers are budgeted for: 4
+// (64 registers) up to 9 ranks, where it needs no spill; the BF16 8-rank
+// reduce then runs 6-10% faster than at the 80 registers (3 CTAs per SM)
+// the compiler picks on its own (GB300, 8 x 8 Mi and 8 x 64 Mi elements).
+// More ranks: 3 (10-11 ranks) or 2, the budgets of the registers they use
+// unbudgeted (80, and 111-128).
+template <int N>
+constexpr int reduce_min_ctas()
+{
+    return N <= 9 ? 4 : (N <= 11 ? 3 : 2);
+}
+
 template <int N, int DT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, reduce_min_ctas<N>())
 reduce_kernel(const __grid_constant__ ReduceParams p, void *out, size_t n, size_t items)
 {
     wait_prior_grid();

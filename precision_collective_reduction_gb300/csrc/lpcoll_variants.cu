@@ -95,8 +95,10 @@ dequantize_fmt_kernel(const uint8_t *codes, const float *scales, void *out, size
     }
 }
 
+// Registers budgeted for 4 resident CTAs per SM (64, no spill), as the main
+// reduce kernel up to 9 ranks; the compiler alone picks 80 (3 CTAs per SM).
 template <int DT, int FMT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 reduce_fmt_kernel(const __grid_constant__ ReduceParams p, int nranks, void *out, size_t n,
                   int block_shift, size_t items)
 {
