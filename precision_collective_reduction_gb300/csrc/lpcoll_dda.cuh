@@ -410,6 +410,45 @@ dda_kernel(const __grid_constant__ DdaParams p, size_t n, size_t full_units,
         dda_unit<N, DT, MODE, false>(p, n, full_units, lane);
 }
 
+// The direct path of dda_kernel with registers budgeted for 3 resident CTAs
+// per SM (at most 80; a few bytes of spill). Left to itself the compiler
+// gives the FP32 kernels of 14-16 ranks 84-98 registers, which leaves 2 CTAs
+// per SM; with the budget they ran 4-7% faster on GB300 (2 GiB of input:
+// 16 ranks flat 735.9 -> 705.2 us, 15 ranks tree 793.3 -> 742.0 us, 14 ranks
+// tree 785.0 -> 735.9 us). 13 ranks and below, and BF16 at 12 and 16 ranks,
+// were equal or slower with it. The loop repeats dda_kernel's instead of
+// sharing a device function with it: with the loop in a shared function the
+// compiler gave the BF16 8-rank kernels 65-68 registers instead of 64, one
+// resident CTA per SM fewer.
+template <int N, int DT, int MODE>
+__global__ void __launch_bounds__(kThreads, 3)
+dda_kernel_r3(const __grid_constant__ DdaParams p, size_t n, size_t full_units,
+              size_t total_units)
+{
+    wait_prior_grid();
+    constexpr int K = units_per_iter<N>();
+    const int lane = threadIdx.x & 31;
+    const size_t warp = (static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const size_t nwarps = (static_cast<size_t>(gridDim.x) * kThreads) >> 5;
+    size_t u = warp;
+    if constexpr (K > 1) {
+        const size_t groups = full_units / K;
+        for (size_t g = warp; g < groups; g += nwarps)
+            dda_units<N, DT, MODE, K>(p, g * K, lane);
+        u = groups * K + warp;
+    }
+    for (; u < full_units; u += nwarps)
+        dda_unit<N, DT, MODE, true>(p, n, u, lane);
+    if (total_units > full_units && warp == full_units % nwarps)
+        dda_unit<N, DT, MODE, false>(p, n, full_units, lane);
+}
+
+template <int N, int DT, int MODE>
+constexpr bool register_budget_3()
+{
+    return DT == LPCOLL_F32 && N >= 14 && (MODE == kFlat || MODE == kTree);
+}
+
 // Units of a message of n elements: all full units, then the ragged one.
 template <int DT>
 inline void unit_counts(size_t n, size_t &full, size_t &total)
@@ -456,8 +495,10 @@ cudaError_t launch_dda_n(const DdaParams &p, size_t n, cudaStream_t stream)
         }
     }
     const size_t K = units_per_iter<N>();
-    return launch_kernel(dda_kernel<N, DT, MODE, false>, item_ctas((total + K - 1) / K), stream,
-                         p, n, full, total);
+    const int grid = item_ctas((total + K - 1) / K);
+    if constexpr (register_budget_3<N, DT, MODE>())
+        return launch_kernel(dda_kernel_r3<N, DT, MODE>, grid, stream, p, n, full, total);
+    return launch_kernel(dda_kernel<N, DT, MODE, false>, grid, stream, p, n, full, total);
 }
 
 template <int DT, int MODE>
