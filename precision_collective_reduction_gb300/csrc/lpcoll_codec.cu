@@ -22,10 +22,11 @@
 
 namespace lpc {
 
-// Units per loop iteration of the dequantize kernel; all loads of an
-// iteration are issued before any of its units is processed (+52% over one
-// unit per iteration on GB300; 8 units: slower).
-constexpr int kDequantizeUnits = 4;
+// Units per warp item of the dequantize kernel; all loads of an item are
+// issued before any of its units is processed. With the one-warp-per-item
+// grid, 2 units measured 1-3% faster per call than 4 or 8 on GB300 (64 Mi
+// FP32 49.8 against 50.2 us in a CUDA graph) and 1 unit 13-28% slower.
+constexpr int kDequantizeUnits = 2;
 // Warp-units [u0, u0 + K) of one message of n elements; e0 / cnt per lane.
 template <int DT, int K>
 __device__ __forceinline__ void unit_lanes(size_t n, size_t u0, int lane, size_t (&e0)[K],

@@ -258,13 +258,14 @@ alltoall_kernel(const __grid_constant__ DdaParams p, int nranks, size_t c, size_
 
 // Low-precision AlltoAll, per element format: wide items per warp step (all
 // their loads issued first) and the resident CTAs per SM the registers are
-// budgeted for (__launch_bounds__). Measured on GB300 with 8 ranks, on grids
-// of that many resident CTAs per SM: FP32 1 item at 3 CTAs per SM (2 CTAs:
-// -17%; 2 items: -1%), BF16 2 items at 4 CTAs per SM (1 item: -20%; 4 items:
-// -3%; 3 CTAs: -4%). The grid has one warp per step (item_ctas).
+// budgeted for (__launch_bounds__). The grid has one warp per step
+// (item_ctas). Measured on GB300 with 8 ranks and that grid: FP32 2 items at
+// 3 CTAs per SM (chunks of 8 Mi: 674.4 us against 688.8 us with 1 item, 705
+// with 4), BF16 2 items at 4 CTAs per SM (1 item: -18%; 4 items at 3 CTAs:
+// -2% at chunks of 1 Mi, +1% at 4 Mi).
 template <int DT> struct A2aLp;
 template <> struct A2aLp<LPCOLL_F32> {
-    static constexpr int kItems = 1;
+    static constexpr int kItems = 2;
     static constexpr int kCtas = 3;
 };
 template <> struct A2aLp<LPCOLL_BF16> {
