@@ -11,12 +11,12 @@ Algorithm choice (host logic only; the work runs in liblpcoll's kernels):
   ``LPCOLL_LP_MIN_BYTES`` bytes (default 16 MiB, the pages' threshold for the
   low-precision collectives); smaller messages are reduced exactly.
 - ``algo``: "flat", "tree", or "auto". The pages place tree at
-  somewhat larger messages than flat. Measured on one GB300 with 8 emulated ranks
-  (BF16, 8 KiB to 128 MiB per rank), flat is never slower than tree: the
-  exact tree is the same kernel, and the low-precision tree adds a
-  requantization and a shard wire (3-16% slower from 2 MiB up). So "auto"
-  means flat unless ``LPCOLL_TREE_MIN_BYTES`` sets a message size from which
-  to use tree.
+  somewhat larger messages than flat. Measured on one GB300 with 8 emulated
+  ranks (BF16, 8 KiB to 256 MiB per rank), flat is never slower than tree:
+  the exact tree is the same kernel, and the low-precision tree adds a
+  requantization and a shard wire (equal up to 8 MiB, 2-3% slower from
+  32 MiB up). So "auto" means flat unless ``LPCOLL_TREE_MIN_BYTES`` sets a
+  message size from which to use tree.
 """
 import os
 
