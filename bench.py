@@ -754,7 +754,8 @@ def run_ours(args):
         extras["decode"] = measure_small(torch, W.DECODE_EXACT_FLAT_N8_BF16, stream,
                                          iters=50, graph_replays=1000)["flat"]
         extras["workloads"] = {
-            wl.name: measure_small(torch, wl, stream, iters=20)
+            wl.name: measure_small(torch, wl, stream, iters=20,
+                                   graph_replays=200 if wl is W.LP_FLAT_N2_1M_F32 else 0)
             for wl in (W.LP_FLAT_N2_1M_F32, W.LP_FLAT_N8_16MB_BF16,
                        W.LP_TREE_N8_64MB_BF16)}
         extras["collectives_lp_n8_16MiB_bf16"] = measure_collectives(torch, stream)
