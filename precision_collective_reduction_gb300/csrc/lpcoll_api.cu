@@ -159,9 +159,9 @@ int dda_common(const void *const *in, void *const *out, int nranks, size_t n,
 // Checks shared by the collectives other than the allreduce; fills the
 // per-rank pointers of p. out[r] may be NULL where out_empty(r) is true.
 template <class Empty>
-int collective_args(const void *const *in, void *const *out, int nranks, int dtype,
-                    int block, uint8_t *const *wire_codes, float *const *wire_scales,
-                    Empty out_empty, DdaParams &p)
+int collective_args(const void *const *in, void *const *out, int nranks, int block,
+                    uint8_t *const *wire_codes, float *const *wire_scales, Empty out_empty,
+                    DdaParams &p)
 {
     int out_st = LPCOLL_OK;
     if (out == nullptr) {
@@ -371,7 +371,7 @@ int reduce_scatter_sim(const void *const *in, void *const *out, int nranks, size
     if (block)
         per = (per + LPCOLL_BLOCK - 1) / LPCOLL_BLOCK * LPCOLL_BLOCK;
     DdaParams p = {};
-    st = collective_args(in, out, nranks, dtype, block, wire_codes, wire_scales,
+    st = collective_args(in, out, nranks, block, wire_codes, wire_scales,
                          [&](int r) { return static_cast<size_t>(r) * per >= n; }, p);
     if (st != LPCOLL_OK)
         return st;
@@ -400,7 +400,7 @@ int all_gather_sim(const void *const *in, void *const *out, int nranks, size_t m
     if (st != LPCOLL_OK || m == 0)
         return st;
     DdaParams p = {};
-    st = collective_args(in, out, nranks, dtype, block, wire_codes, wire_scales,
+    st = collective_args(in, out, nranks, block, wire_codes, wire_scales,
                          [](int) { return false; }, p);
     if (st != LPCOLL_OK)
         return st;
@@ -425,7 +425,7 @@ int all_to_all_sim(const void *const *in, void *const *out, int nranks, size_t c
     if (st != LPCOLL_OK || c == 0)
         return st;
     DdaParams p = {};
-    st = collective_args(in, out, nranks, dtype, block, wire_codes, wire_scales,
+    st = collective_args(in, out, nranks, block, wire_codes, wire_scales,
                          [](int) { return false; }, p);
     if (st != LPCOLL_OK)
         return st;
