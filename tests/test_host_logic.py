@@ -76,6 +76,14 @@ def test_staged_bytes():
     assert bench.staged_bytes("lp_quantize", N, n, 4) == 4 * n + q
     assert bench.staged_bytes("lp_dequantize", N, n, 2) == q + 2 * n
     assert bench.staged_bytes("lp_reduce", N, n, 4) == N * q + 4 * n
+    # the staged chain of the 16 MiB BF16 workload: 8 quantizes (16 MiB read,
+    # 8 Mi codes + 64 Ki scales written each), then the reduce of the 8
+    # payloads into one 16 MiB output
+    n = 8 * (1 << 20)
+    chain = 8 * bench.staged_bytes("lp_quantize", 8, n, 2) + \
+        bench.staged_bytes("lp_reduce", 8, n, 2)
+    assert chain == 8 * (2 * n + n + 4 * (n // 128)) + 8 * (n + 4 * (n // 128)) + 2 * n
+    assert chain == 289_406_976
 
 
 def test_binding_refuses_short_rank_lists():
