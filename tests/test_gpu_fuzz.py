@@ -1,6 +1,10 @@
 """Seeded random configurations of every entry point against the oracle, bit
 for bit: operation, rank count, length (including ragged and tiny), dtype,
-exact or low precision, FP8 format and block size, in place or not."""
+exact or low precision, FP8 format and block size, in place or not.
+
+LPCOLL_FUZZ_CONFIGS sets how many configurations run (default 300)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -16,7 +20,7 @@ NP = {W.F32: np.float32, W.BF16: np.uint16}
 OPS = ["flat", "tree", "rs", "ag", "a2a", "quant", "reduce", "fmt"]
 
 
-def _configs(count=300, seed=2026):
+def _configs(count=int(os.environ.get("LPCOLL_FUZZ_CONFIGS", "300")), seed=2026):
     g = np.random.default_rng(seed)
     for i in range(count):
         op = OPS[i % len(OPS)]
