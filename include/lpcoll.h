@@ -307,8 +307,10 @@ int dda_flat_sim_noalloc(const void *const *in, void *const *out, int nranks,
  * An access outside the list is skipped (a skipped load reads zeros) and
  * recorded; nothing traps, so the CUDA context stays usable. That build
  * allocates one small managed record on first use, copies the buffer list
- * to the device ahead of every launch (so its calls are slower and must
- * not be captured into a CUDA graph), and is for tests only.
+ * to the device ahead of every launch into one list per source file of the
+ * library (so its calls are slower, must not be captured into a CUDA graph,
+ * and must not overlap on the GPU: calls on several streams or threads at
+ * once would check against each other's lists), and is for tests only.
  *
  * lpcoll_debug_bounds_errors waits for the device (cudaDeviceSynchronize)
  * and returns 1 if any access failed its check since the previous call
