@@ -397,6 +397,7 @@ def measure_small(torch, w, stream, iters, graph_replays=0):
         us = flushed_median_us(torch, stream, scratch, lambda: bufs.run(algo, s), iters)
         nbytes = bytes_alg(w.nranks, w.n, w.elem_bytes, w.block, algo)
         res = {"us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
+               "frac_of_peak": round(nbytes / us / 1e3 / measured_peaks()[0], 4),
                "bytes_alg": nbytes, "l2": "flushed"}
         # warm L2: back-to-back calls, no flush (what a chain of calls costs)
         warm_calls = 200
@@ -485,7 +486,8 @@ def measure_collectives(torch, stream, iters=20):
                      "warm_us_per_call": round(back_to_back_us(torch, stream,
                                                                lambda: fn(stream), 100), 3),
                      "graph_us_per_call": round(gus, 3),
-                     "graph_GBps": round(nbytes / gus / 1e3, 1)}
+                     "graph_GBps": round(nbytes / gus / 1e3, 1),
+                     "graph_frac_of_peak": round(nbytes / gus / 1e3 / measured_peaks()[0], 4)}
     del ins, wc, ws, scratch, rs_out, full_out
     torch.cuda.empty_cache()
     return out
