@@ -7,8 +7,12 @@ blocks, the ragged tail if any, and random blocks): blocks are independent in
 every stage, so the oracle run on the gathered blocks of every rank computes
 exactly those blocks of the full result. On the whole message the test checks
 properties that hold at any size: all N outputs identical, every scale finite
-and non-negative.
+and non-negative. With LPCOLL_FULL_ORACLE=1 every workload is also compared
+with the oracle run on the whole message, element by element (about a
+minute of oracle time on one core).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -84,6 +88,38 @@ def test_workload(oracle, w):
         if w.block and algo == "tree":
             _check(pick(bufs.shard_codes), o_sc, "shard_codes")
             _check(pick_s(bufs.shard_scales), o_ss, "shard_scales")
+    del bufs
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.skipif(os.environ.get("LPCOLL_FULL_ORACLE") != "1",
+                    reason="whole-message oracle comparison: set LPCOLL_FULL_ORACLE=1 "
+                           "(about a minute of CPU oracle time)")
+@pytest.mark.parametrize("w", W.WORKLOADS, ids=[w.name for w in W.WORKLOADS])
+def test_workload_full_oracle(oracle, w):
+    """Every element of every output, wire payload and shard payload of the
+    full-size workload against the oracle run on the whole message."""
+    ins = W.draw_all(w)
+    bufs = runner.RankBuffers(w.nranks, w.n, w.dtype, w.block, separate_tree_out=True)
+    bufs.load(ins)
+    stream = torch.cuda.current_stream().cuda_stream
+    for algo in w.algos:
+        bufs.run(algo, stream)
+        torch.cuda.synchronize()
+        if algo == "tree":
+            o_out, o_wc, o_ws, o_sc, o_ss = oracle.tree(ins, block=w.block)
+        else:
+            o_out, o_wc, o_ws = oracle.flat(ins, block=w.block)
+        outs = bufs.tree_outs if algo == "tree" else bufs.outs
+        for r in range(w.nranks):
+            _check(from_dev(outs[r]), o_out[r], "%s out[%d]" % (algo, r))
+            if w.block:
+                _check(from_dev(bufs.wire_codes[r]), o_wc[r], "%s wire_codes[%d]" % (algo, r))
+                _check(from_dev(bufs.wire_scales[r]), o_ws[r], "%s wire_scales[%d]" % (algo, r))
+        if w.block and algo == "tree":
+            _check(from_dev(bufs.shard_codes), o_sc, "shard_codes")
+            _check(from_dev(bufs.shard_scales), o_ss, "shard_scales")
+        del o_out
     del bufs
     torch.cuda.empty_cache()
 
