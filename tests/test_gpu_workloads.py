@@ -7,9 +7,9 @@ blocks, the ragged tail if any, and random blocks): blocks are independent in
 every stage, so the oracle run on the gathered blocks of every rank computes
 exactly those blocks of the full result. On the whole message the test checks
 properties that hold at any size: all N outputs identical, every scale finite
-and non-negative. With LPCOLL_FULL_ORACLE=1 every workload is also compared
-with the oracle run on the whole message, element by element (about a
-minute of oracle time on one core).
+and non-negative. With LPCOLL_FULL_ORACLE=1 every workload, the collectives
+and the variants are also compared with the oracle run on the whole message,
+element by element (about a minute of oracle time on one core).
 """
 import os
 
@@ -124,6 +124,50 @@ def test_workload_full_oracle(oracle, w):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.skipif(os.environ.get("LPCOLL_FULL_ORACLE") != "1",
+                    reason="whole-message oracle comparison: set LPCOLL_FULL_ORACLE=1")
+@pytest.mark.parametrize("kind", ["reduce_scatter", "all_gather", "all_to_all"])
+def test_collectives_full_oracle(oracle, kind):
+    """The collectives in the benchmark's configuration (8 ranks, 16 MiB BF16
+    per rank, low precision): every element of every output, wire code and
+    scale against the oracle run on the whole message."""
+    import precision_collective_reduction_gb300 as pcr
+    w = W.LP_FLAT_N8_16MB_BF16
+    N, n = w.nranks, w.n
+    ins = W.draw_all(w)
+    dins = [torch.from_numpy(x).view(torch.int16).view(torch.bfloat16).cuda() for x in ins]
+    nb = pcr.nblocks(n)
+    wc = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(N)]
+    ws = [torch.empty(N * nb, dtype=torch.float32, device="cuda") for _ in range(N)]
+    if kind == "reduce_scatter":
+        per = pcr.shard_len(n, N)
+        outs = [torch.empty(max(1, min(per, n - r * per)), dtype=torch.bfloat16, device="cuda")
+                for r in range(N)]
+        pcr.reduce_scatter_sim(dins, outs, wire_codes=wc, wire_scales=[t[:nb] for t in ws])
+        o_out, o_wc, o_ws = oracle.reduce_scatter(ins)
+        ncode, nscale = n, nb
+    elif kind == "all_gather":
+        m = n // N
+        outs = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+        pcr.all_gather_sim([t[:m] for t in dins], outs, wire_codes=[t[:m] for t in wc],
+                           wire_scales=[t[:pcr.nblocks(m)] for t in ws])
+        o_out, o_wc, o_ws = oracle.all_gather([x[:m] for x in ins])
+        ncode, nscale = m, pcr.nblocks(m)
+    else:
+        c = n // N
+        outs = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+        pcr.all_to_all_sim(dins, outs, wire_codes=wc, wire_scales=ws)
+        o_out, o_wc, o_ws = oracle.all_to_all(ins)
+        ncode, nscale = n, N * pcr.nblocks(c)
+    torch.cuda.synchronize()
+    for r in range(N):
+        _check(from_dev(outs[r])[:o_out[r].size], o_out[r], "%s out[%d]" % (kind, r))
+        _check(from_dev(wc[r][:ncode]), o_wc[r][:ncode], "%s wire_codes[%d]" % (kind, r))
+        _check(from_dev(ws[r][:nscale]), o_ws[r][:nscale], "%s wire_scales[%d]" % (kind, r))
+    del dins, wc, ws, outs
+    torch.cuda.empty_cache()
+
+
 def test_collectives_at_benchmark_size(oracle):
     """ReduceScatter, AllGather and AlltoAll in the benchmark's configuration
     (8 ranks, 16 MiB BF16 per rank, low precision), checked on sampled
@@ -216,5 +260,36 @@ def test_variants_at_benchmark_size(oracle, fmt, block):
             _check(from_dev(scales[r][b:b + 1]), pays[r][1], "scale r=%d b=%d" % (r, b))
         want = oracle.reduce_fmt([c for c, _ in pays], [s for _, s in pays], block, fmt)
         _check(from_dev(out[lo:hi]), want, "reduced b=%d" % b)
+    del dins, codes, scales, out
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.skipif(os.environ.get("LPCOLL_FULL_ORACLE") != "1",
+                    reason="whole-message oracle comparison: set LPCOLL_FULL_ORACLE=1")
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("block", [32, 64, 128, 256])
+def test_variants_full_oracle(oracle, fmt, block):
+    """The format / block-size ablation's configuration (8 ranks x 4 Mi FP32):
+    every code and scale of every rank's payload and every element of the
+    reduced result against the oracle."""
+    import precision_collective_reduction_gb300 as pcr
+    w = W.LP_GRAD_N8_256MB_F32
+    n = 1 << 22
+    ins = W.draw_all(w, n)
+    dins = [torch.from_numpy(x).cuda() for x in ins]
+    codes = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(w.nranks)]
+    scales = [torch.empty(pcr.nblocks(n, block), dtype=torch.float32, device="cuda")
+              for _ in range(w.nranks)]
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    for r in range(w.nranks):
+        pcr.lp_quantize_fmt(dins[r], codes[r], scales[r], block, fmt)
+    pcr.lp_reduce_fmt(codes, scales, out, block, fmt)
+    torch.cuda.synchronize()
+    pays = [oracle.quantize_fmt(x, block, fmt) for x in ins]
+    for r in range(w.nranks):
+        _check(from_dev(codes[r]), pays[r][0], "codes[%d]" % r)
+        _check(from_dev(scales[r]), pays[r][1], "scales[%d]" % r)
+    want = oracle.reduce_fmt([c for c, _ in pays], [s for _, s in pays], block, fmt)
+    _check(from_dev(out), want, "reduced")
     del dins, codes, scales, out
     torch.cuda.empty_cache()
