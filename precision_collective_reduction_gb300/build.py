@@ -6,6 +6,7 @@ this file. A stamp of the sources and flags skips the build when nothing
 changed.
 """
 import concurrent.futures as cf
+import fcntl
 import hashlib
 import os
 import shutil
@@ -60,17 +61,25 @@ def _digest(extra):
 
 def build(force: bool = False, extra_flags=(), debug_bounds: bool = False) -> str:
     """Compile and link liblpcoll.so (debug_bounds: the bounds-checked
-    liblpcoll_debug_bounds.so); returns its path."""
+    liblpcoll_debug_bounds.so); returns its path. Processes that build at
+    the same time (the ranks of a torchrun launch) take turns on a lock
+    file, and all but the first find the library up to date."""
     flags = NVCC_FLAGS + list(extra_flags) + (["-DLPCOLL_DEBUG_BOUNDS"] if debug_bounds else [])
     build_dir = DEBUG_BUILD if debug_bounds else BUILD
     lib = DEBUG_LIB if debug_bounds else LIB
+    os.makedirs(build_dir, exist_ok=True)
+    with open(os.path.join(build_dir, "lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        return _build_locked(force, flags, build_dir, lib)
+
+
+def _build_locked(force, flags, build_dir, lib):
     stamp = os.path.join(build_dir, "stamp")
     digest = _digest(flags)
     if not force and os.path.exists(lib) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == digest:
                 return lib
-    os.makedirs(build_dir, exist_ok=True)
     exe = nvcc()
 
     def compile_one(src):
